@@ -1,0 +1,108 @@
+"""Seeded synthetic workloads for the gated delta-rule prefill and decode step.
+
+This module only draws random inputs; it holds none of the method's arithmetic
+and is shared by the tests, the benchmark and the smoke check (both the CUDA
+path and the CPU oracle consume what it returns).
+
+Recipe (one ``torch.Generator`` per workload, seeded with the workload's seed,
+tensors drawn on the CPU in this fixed order: q, k, v, g_log, beta, state):
+
+* q, k  ~ N(0, 1) in fp32, then divided by their L2 norm over the head dim
+  (the "GDN CTE Kernel API Reference" Notes require L2-normalised q/k), then
+  rounded to the compute dtype (round-to-nearest-even for bf16);
+* v     ~ N(0, 1), rounded to the compute dtype;
+* g_log ~ U(lo, hi) fp32 (a negative log-decay, Parameters / g_log);
+* beta  = sigmoid(N(0, s)) fp32, in (0, 1) (Parameters / beta);
+* state ~ N(0, sigma) fp32 [B, Hv, Dk, Dv] when the workload supplies one,
+  otherwise the zero-start ("omitted") form is used.
+
+``N(m, s)`` names a standard deviation ``s``.
+"""
+from __future__ import annotations
+
+import dataclasses
+import math
+
+import torch
+
+
+@dataclasses.dataclass(frozen=True)
+class Workload:
+    name: str
+    kind: str            # "prefill" or "decode"
+    B: int
+    Hk: int
+    Hv: int
+    S: int
+    Dk: int
+    Dv: int
+    dtype: str           # compute dtype of q/k/v/out: "f32" or "bf16"
+    g_lo: float
+    g_hi: float
+    beta_std: float
+    state_std: float     # 0.0 -> zero initial state (no state supplied)
+    seed: int
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.Dk)
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.S
+
+    def with_(self, **kw) -> "Workload":
+        return dataclasses.replace(self, **kw)
+
+
+# The five workloads of the method's benchmark plan.
+TINY_PREFILL = Workload("prefill_b1_h2_s128_d64_f32", "prefill", 1, 2, 2, 128, 64, 64, "f32",
+                        -0.5, -0.005, 1.0, 0.0, 0)
+DECODE_STEP = Workload("decode_b64_hk16_hv32_d128_bf16", "decode", 64, 16, 32, 1, 128, 128, "bf16",
+                       -0.5, -0.005, 1.0, 0.02, 1)
+PREFILL = Workload("prefill_b4_hk16_hv32_s4096_d128_bf16", "prefill", 4, 16, 32, 4096, 128, 128, "bf16",
+                   -0.5, -0.005, 1.0, 0.02, 2)
+LONG_PREFILL = Workload("prefill_b1_hk16_hv32_s32768_d128_bf16", "prefill", 1, 16, 32, 32768, 128, 128,
+                        "bf16", -0.5, -0.005, 1.0, 0.0, 3)
+WIDE_GQA_PREFILL = Workload("prefill_b16_hk8_hv32_s2048_d128_bf16", "prefill", 16, 8, 32, 2048, 128, 128,
+                            "bf16", -2.0, -0.001, 2.0, 0.05, 4)
+
+ALL = [TINY_PREFILL, DECODE_STEP, PREFILL, LONG_PREFILL, WIDE_GQA_PREFILL]
+BY_NAME = {w.name: w for w in ALL}
+
+
+def make_inputs(w: Workload, device="cpu", pin: bool = False):
+    """Draw the workload's tensors.  Returns a dict with q, k, v, g_log, beta,
+    state (None for a zero start) and scale.  Values are drawn on the CPU so they
+    do not depend on the device; they are then moved to ``device``."""
+    gen = torch.Generator(device="cpu").manual_seed(w.seed)
+    dt = w.torch_dtype
+
+    def unit(shape):
+        x = torch.randn(shape, generator=gen, dtype=torch.float32)
+        x = x / x.norm(dim=-1, keepdim=True).clamp_min(1e-30)
+        return x.to(dt)
+
+    q = unit((w.B, w.Hk, w.S, w.Dk))
+    k = unit((w.B, w.Hk, w.S, w.Dk))
+    v = torch.randn((w.B, w.Hv, w.S, w.Dv), generator=gen, dtype=torch.float32).to(dt)
+    g = torch.rand((w.B, w.Hv, w.S), generator=gen, dtype=torch.float32) * (w.g_hi - w.g_lo) + w.g_lo
+    beta = torch.sigmoid(torch.randn((w.B, w.Hv, w.S), generator=gen, dtype=torch.float32) * w.beta_std)
+    state = None
+    if w.state_std > 0.0:
+        state = torch.randn((w.B, w.Hv, w.Dk, w.Dv), generator=gen, dtype=torch.float32) * w.state_std
+    out = dict(q=q, k=k, v=v, g_log=g, beta=beta, state=state, scale=w.scale)
+    for key in ("q", "k", "v", "g_log", "beta", "state"):
+        t = out[key]
+        if t is None:
+            continue
+        if pin:
+            t = t.pin_memory()
+        if device != "cpu":
+            t = t.to(device)
+        out[key] = t
+    return out
