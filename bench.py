@@ -1,0 +1,396 @@
+"""Benchmark of the gated delta-rule prefill and decode step on one GB300 per rank.
+
+One JSON line on rank 0.  ``value`` is the prefill throughput (tokens/s =
+B * S / time, summed over ranks) on the B=4, Hk=16, Hv=32, S=4096, Dk=Dv=128
+bf16 workload with its inputs resident in HBM; the decode step (B=64, Hk=16,
+Hv=32, Dk=Dv=128, 128 MiB fp32 state) is measured in the same run and
+reported under ``decode`` in GB/s of algorithmic traffic.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun each rank runs its own copy of the workload (independent
+sequences, no collective): weak scaling.  ``--impl reference`` times the fp64
+CPU oracle on bounded samples of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import workloads  # noqa: E402
+
+METRIC = "GDN prefill tokens/s + tensor-pipe %; decode-step state GB/s vs HBM peak"
+PREFILL = workloads.PREFILL
+DECODE = workloads.DECODE_STEP
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.md")
+KERNEL_SOURCES = {
+    "gdn_prefill_tc_kernel": "gated_delta_rule_20_gb300/csrc/prefill_tc.cu",
+    "gdn_decode_kernel": "gated_delta_rule_20_gb300/csrc/decode.cu",
+}
+
+
+# ------------------------------------------------------------------ algorithmic accounting
+def prefill_bytes(w) -> int:
+    """Bytes the method must move once: q, k per key head; v, out per value
+    head; g_log and beta; the fp32 state in (when supplied) and out."""
+    e = 2 if w.dtype == "bf16" else 4
+    qk = 2 * w.B * w.Hk * w.S * w.Dk * e
+    v_out = 2 * w.B * w.Hv * w.S * w.Dv * e
+    gb = 2 * w.B * w.Hv * w.S * 4
+    st = (2 if w.state_std > 0 else 1) * w.B * w.Hv * w.Dk * w.Dv * 4
+    return qk + v_out + gb + st
+
+
+def prefill_flops(w, C=64) -> float:
+    """Algorithmic flops at chunk C with causal triangles counted at half:
+    per value-head token 6 Dk Dv + C (3 Dk + 2 Dv) + C^2 / 3."""
+    per = 6 * w.Dk * w.Dv + C * (3 * w.Dk + 2 * w.Dv) + C * C / 3.0
+    return per * w.B * w.Hv * w.S
+
+
+def decode_bytes(w) -> int:
+    e = 2 if w.dtype == "bf16" else 4
+    return (2 * w.B * w.Hv * w.Dk * w.Dv * 4 + 2 * w.B * w.Hk * w.Dk * e + 2 * w.B * w.Hv * w.Dv * e
+            + 2 * w.B * w.Hv * 4)
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm=float(p["hbm_gbs"]), bf16=float(p["bf16_tflops"]),
+                    bf16_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), source="measured")
+    return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
+
+
+def recorded_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current source of the kernel (else None)."""
+    import hashlib
+    if not os.path.exists(PROFILE_TRAFFIC):
+        return None
+    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
+    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    for line in open(PROFILE_TRAFFIC):
+        parts = line.strip().strip("|").split("|")
+        parts = [p.strip() for p in parts]
+        if len(parts) >= 3 and parts[0] == kernel and parts[2] == sha:
+            try:
+                return int(parts[1])
+            except ValueError:
+                return None
+    return None
+
+
+# ------------------------------------------------------------------ clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = os.path.join("/tmp", "gdn_clocks_%d_%d.csv" % (os.getpid(), gpu_index))
+
+    def __enter__(self):
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            p = [x.strip() for x in line.split(",")]
+            if len(p) < 9:
+                continue
+            try:
+                sm.append(float(p[1]))
+                mx.append(float(p[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, p[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        os.unlink(self.path)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------ CPU oracle baseline
+def oracle_sample(w, n_seq: int, seed: int = 0):
+    """Oracle inputs for the first n_seq (batch, value-head) sequences of the workload."""
+    import torch
+    x = workloads.make_inputs(w)
+    G = w.Hv // w.Hk
+    heads = [(i // w.Hv, i % w.Hv) for i in range(n_seq)]
+    pick = lambda t, kv: torch.stack([t[b, (h // G) if kv else h] for b, h in heads]).unsqueeze(1)
+    return dict(q=pick(x["q"], True).double().numpy(), k=pick(x["k"], True).double().numpy(),
+                v=pick(x["v"], False).double().numpy(), g=pick(x["g_log"], False).double().numpy(),
+                beta=pick(x["beta"], False).double().numpy(),
+                state=None if x["state"] is None else pick(x["state"], False).double().numpy(),
+                scale=x["scale"])
+
+
+def time_oracle(w, n_seq: int, sample=None):
+    import oracle
+    s = sample if sample is not None else oracle_sample(w, n_seq)
+    t0 = time.perf_counter()
+    oracle.recurrence(s["q"], s["k"], s["v"], s["g"], s["beta"], s["scale"], s["state"])
+    dt = time.perf_counter() - t0
+    full_time = dt * (w.B * w.Hv) / n_seq       # the whole workload at this rate
+    return dict(seconds=dt, tokens_per_s=w.B * w.S / full_time, cores=oracle.max_threads())
+
+
+# ------------------------------------------------------------------ our implementation
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import gated_delta_rule_20_gb300 as gdn
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    peaks = load_peaks()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # ---------------- prefill, inputs resident in HBM
+    w = PREFILL.with_(seed=PREFILL.seed + 1000 * rank)
+    x = workloads.make_inputs(w, device=dev)
+    state = x["state"].clone()
+    out = torch.empty((w.B, w.Hv, w.S, w.Dv), dtype=w.torch_dtype, device=dev)
+
+    def prefill_step():
+        gdn.prefill(x["q"], x["k"], x["v"], x["g_log"], x["beta"], x["scale"], state, out, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        prefill_step()
+    torch.cuda.synchronize()
+    if gdn.device_status(local_rank) != 0:
+        raise RuntimeError("prefill kernel reported a wait timeout")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clk:
+        barrier()
+        torch.cuda.synchronize()
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            prefill_step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        barrier()
+    clocks = clk.summary()
+    launch_ms = [a.elapsed_time(b) for a, b in ev]
+    total_ms = ev[0][0].elapsed_time(ev[-1][1])
+    ms_per_step = total_ms / args.steps
+    if world > 1:
+        t = torch.tensor([ms_per_step], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_per_step = float(t.item())
+    value = w.B * w.S * world / (ms_per_step * 1e-3)
+    avg_launch_s = statistics.mean(launch_ms) * 1e-3
+    pbytes = prefill_bytes(w)
+    pflops = prefill_flops(w)
+    roof = {"bound": "hbm", "achieved": pbytes / avg_launch_s / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+            "frac": pbytes / avg_launch_s / 1e9 / peaks["hbm"], "traffic": recorded_traffic("gdn_prefill_tc_kernel"),
+            "kernel": "gdn_prefill_tc_kernel", "algorithmic_bytes_per_launch": pbytes,
+            "peak_source": peaks["source"] + " hbm_gbs",
+            "tensor": {"achieved_tflops": pflops / avg_launch_s / 1e12, "peak": peaks["bf16_sustained"],
+                       "frac": pflops / avg_launch_s / 1e12 / peaks["bf16_sustained"],
+                       "algorithmic_flops_per_launch": pflops}}
+
+    # ---------------- decode step, L2 flushed between launches
+    wd = DECODE.with_(seed=DECODE.seed + 1000 * rank)
+    xd = workloads.make_inputs(wd, device=dev)
+    dstate = xd["state"].clone()
+    dout = torch.empty((wd.B, wd.Hv, 1, wd.Dv), dtype=wd.torch_dtype, device=dev)
+    flush = torch.empty(256 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
+
+    def decode_step():
+        gdn.decode_step(xd["q"], xd["k"], xd["v"], xd["g_log"], xd["beta"], xd["scale"], dstate, dout,
+                        stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        decode_step()
+    torch.cuda.synchronize()
+    dev_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        dev_ev[i][0].record(stream)
+        decode_step()
+        dev_ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    dms = statistics.median([a.elapsed_time(b) for a, b in dev_ev])
+    dbytes = decode_bytes(wd)
+    decode = {"value": dbytes / (dms * 1e-3) / 1e9 * world, "unit": "GB/s", "ms": dms,
+              "workload": wd.name, "l2": "flushed (256 MiB write) before every launch",
+              "roofline": {"bound": "hbm", "achieved": dbytes / (dms * 1e-3) / 1e9, "peak": peaks["hbm"],
+                           "unit": "GB/s", "frac": dbytes / (dms * 1e-3) / 1e9 / peaks["hbm"],
+                           "traffic": recorded_traffic("gdn_decode_kernel"), "kernel": "gdn_decode_kernel",
+                           "algorithmic_bytes_per_launch": dbytes}}
+    del xd, dstate, dout, flush
+
+    # ---------------- end to end through the public API from pinned host buffers
+    xh = {k: (v.to("cpu").pin_memory() if hasattr(v, "to") and v is not None else v) for k, v in x.items()}
+    st_h = xh["state"].clone().pin_memory()
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    st_back = torch.empty(st_h.shape, dtype=torch.float32).pin_memory()
+    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
+    dg, db, dst = torch.empty_like(x["g_log"]), torch.empty_like(x["beta"]), torch.empty_like(state)
+    h2d = sum(t.numel() * t.element_size() for t in (xh["q"], xh["k"], xh["v"], xh["g_log"], xh["beta"], st_h))
+    d2h = out_h.numel() * out_h.element_size() + st_back.numel() * 4
+
+    def e2e_step():
+        for d_, h_ in ((dq, xh["q"]), (dk, xh["k"]), (dv, xh["v"]), (dg, xh["g_log"]), (db, xh["beta"]),
+                       (dst, st_h)):
+            d_.copy_(h_, non_blocking=True)
+        gdn.prefill(dq, dk, dv, dg, db, x["scale"], dst, out, stream=stream)
+        out_h.copy_(out, non_blocking=True)
+        st_back.copy_(dst, non_blocking=True)
+
+    for _ in range(max(args.warmup, 3)):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(1, min(args.steps, 10))
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    e2e = {"value": w.B * w.S * world / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    if gdn.device_status(local_rank) != 0:
+        raise RuntimeError("a kernel reported a wait timeout")
+
+    result = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hk": w.Hk, "Hv": w.Hv, "S": w.S, "Dk": w.Dk, "Dv": w.Dv,
+                   "parallelism": "independent sequences per rank" if world > 1 else "single gpu",
+                   "l2": "inputs larger than L2 (%.0f MB per step)" % (pbytes / 1e6)},
+        "roofline": roof, "decode": decode, "e2e": e2e, "clocks": clocks,
+        "gpu_launches": args.steps * gdn.kernels_per_call(),
+        "launch_ms": {"median": statistics.median(launch_ms), "min": min(launch_ms), "max": max(launch_ms)},
+    }
+    if rank == 0 and world == 1:
+        n_seq = args.oracle_sequences
+        r = time_oracle(w, n_seq)
+        result["cpu_baseline"] = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": r["cores"],
+                                  "kind": "oracle",
+                                  "sample": "%d of %d (batch, value-head) sequences, all %d tokens each, "
+                                            "%.1f s wall; scaled to the whole workload" % (
+                                                n_seq, w.B * w.Hv, w.S, r["seconds"])}
+    return result
+
+
+def run_reference(args):
+    """The fp64 CPU oracle timed on bounded samples of the prefill workload."""
+    w = PREFILL
+    n_seq = args.reference_sequences
+    sample = oracle_sample(w, n_seq)
+    for _ in range(args.warmup):
+        time_oracle(w, n_seq, sample)
+    times = []
+    cores = 1
+    for _ in range(args.steps):
+        r = time_oracle(w, n_seq, sample)
+        times.append(r["seconds"])
+        cores = r["cores"]
+    sec = statistics.mean(times)
+    full = sec * (w.B * w.Hv) / n_seq
+    value = w.B * w.S / full
+    desc = ("%d of %d (batch, value-head) sequences x %d tokens per step, scaled to the whole workload"
+            % (n_seq, w.B * w.Hv, w.S))
+    return {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": full * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name, "B": w.B, "Hk": w.Hk, "Hv": w.Hv, "S": w.S, "Dk": w.Dk, "Dv": w.Dv,
+                   "parallelism": "OpenMP over sequences on the host cores"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle", "sample": desc},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--oracle-sequences", type=int, default=32)
+    ap.add_argument("--reference-sequences", type=int, default=8)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        print(json.dumps(run_reference(args)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    res = run_ours(args, rank, world, local_rank)
+    if rank == 0:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

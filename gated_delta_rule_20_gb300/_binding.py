@@ -1,0 +1,174 @@
+"""ctypes binding of ``libgdn.so`` (declared in ``include/gdn.h``).
+
+Argument marshalling only: every step of the computation runs in the library's
+CUDA kernels.  Tensors are PyTorch CUDA tensors (PyTorch supplies device memory
+and streams); the library is called on the current torch stream.  If the
+shared library is missing the binding raises instead of falling back to
+anything else.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(HERE, "libgdn.so")
+
+GDN_OK = 0
+GDN_ERR_NULL = 1
+GDN_ERR_DIMS = 2
+GDN_ERR_UNSUPPORTED = 3
+GDN_ERR_ALIGN = 4
+GDN_ERR_CUDA = 5
+GDN_ERR_TIMEOUT = 6
+
+GDN_F32 = 0
+GDN_BF16 = 1
+
+GDN_ZERO_INITIAL_STATE = 1 << 0
+GDN_FORCE_FFMA = 1 << 1
+
+# Every symbol include/gdn.h declares.
+EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
+            "gdn_device_status", "gdn_kernels_per_call")
+
+
+class GdnDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("Hk", ctypes.c_int64), ("Hv", ctypes.c_int64), ("S", ctypes.c_int64),
+                ("Dk", ctypes.c_int64), ("Dv", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
+
+
+class GdnError(RuntimeError):
+    def __init__(self, code: int, msg: str):
+        super().__init__(msg)
+        self.code = code
+
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load ``libgdn.so`` (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError("libgdn.so is not built (%s); run __graft_entry__.build() or "
+                               "python gated_delta_rule_20_gb300/build.py" % LIB_PATH)
+        L = ctypes.CDLL(LIB_PATH)
+        vp, fp = ctypes.c_void_p, ctypes.c_void_p
+        sig = [vp, vp, vp, fp, fp, ctypes.c_float, fp, vp, ctypes.POINTER(GdnDims), vp]
+        for name in ("gdn_prefill", "gdn_decode_step"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = sig
+        L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(GdnDims)]
+        L.gdn_status_string.restype = ctypes.c_char_p
+        L.gdn_status_string.argtypes = [ctypes.c_int]
+        L.gdn_device_status.restype = ctypes.c_int
+        L.gdn_device_status.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]
+        L.gdn_kernels_per_call.restype = ctypes.c_int
+        L.gdn_kernels_per_call.argtypes = []
+        _lib = L
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return lib().gdn_status_string(int(code)).decode()
+
+
+def make_dims(B, Hk, Hv, S, Dk, Dv, dtype, flags=0) -> GdnDims:
+    return GdnDims(int(B), int(Hk), int(Hv), int(S), int(Dk), int(Dv), int(dtype), int(flags))
+
+
+def _check(code: int):
+    if code != GDN_OK:
+        raise GdnError(code, status_string(code))
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t) -> int:
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return GDN_BF16
+    if t.dtype == torch.float32:
+        return GDN_F32
+    raise TypeError("q/k/v must be bfloat16 or float32, got %s" % t.dtype)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, force_ffma, stream):
+    torch = _torch()
+    for nm, t in (("q", q), ("k", k), ("v", v), ("g_log", g_log), ("beta", beta), ("state", state), ("out", out)):
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % nm)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % nm)
+    if g_log.dtype != torch.float32 or beta.dtype != torch.float32 or state.dtype != torch.float32:
+        raise TypeError("g_log, beta and state must be float32")
+    dt = _dtype_code(q)
+    if k.dtype != q.dtype or v.dtype != q.dtype or out.dtype != q.dtype:
+        raise TypeError("q, k, v and out must share the compute dtype")
+    if q.dim() != 4 or v.dim() != 4:
+        raise ValueError("q/k must be [B,Hk,S,Dk] and v [B,Hv,S,Dv]")
+    B, Hk, S, Dk = q.shape
+    Hv, Dv = v.shape[1], v.shape[3]
+    if tuple(k.shape) != tuple(q.shape) or tuple(v.shape[:3]) != (B, Hv, S) or \
+            tuple(g_log.shape) != (B, Hv, S) or tuple(beta.shape) != (B, Hv, S) or \
+            tuple(state.shape) != (B, Hv, Dk, Dv) or tuple(out.shape) != (B, Hv, S, Dv):
+        raise ValueError("inconsistent shapes")
+    flags = (GDN_ZERO_INITIAL_STATE if zero_initial_state else 0) | (GDN_FORCE_FFMA if force_ffma else 0)
+    dims = make_dims(B, Hk, Hv, S, Dk, Dv, dt, flags)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        code = getattr(lib(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(g_log), _ptr(beta), ctypes.c_float(scale),
+                                    _ptr(state), _ptr(out), ctypes.byref(dims), ctypes.c_void_p(stream.cuda_stream))
+    _check(code)
+    return out, state
+
+
+def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=False, stream=None):
+    """Chunked prefill (``gdn_prefill``).
+
+    ``state`` [B,Hv,Dk,Dv] fp32 is updated in place and returned; ``None`` means
+    the zero-start form (a new zero-initialised tensor receives the final
+    state).  Returns ``(out, state)``.
+    """
+    torch = _torch()
+    B, Hk, S, Dk = q.shape
+    Hv, Dv = v.shape[1], v.shape[3]
+    zero = state is None
+    if zero:
+        state = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hv, S, Dv), dtype=q.dtype, device=q.device)
+    return _call("gdn_prefill", q, k, v, g_log, beta, scale, state, out, zero, force_ffma, stream)
+
+
+def decode_step(q, k, v, g_log, beta, scale, state, out=None, *, stream=None):
+    """One token (``gdn_decode_step``): q, k [B,Hk,1,Dk], v [B,Hv,1,Dv],
+    g_log / beta [B,Hv,1]; ``state`` is updated in place.  Returns ``(out, state)``."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty(v.shape, dtype=q.dtype, device=q.device)
+    return _call("gdn_decode_step", q, k, v, g_log, beta, scale, state, out, False, False, stream)
+
+
+def device_status(device: int = 0, clear: bool = True) -> int:
+    """Kernel-side status word of ``device`` (0 = no kernel reported a problem)."""
+    code = ctypes.c_int32(0)
+    _check(lib().gdn_device_status(int(device), 1 if clear else 0, ctypes.byref(code)))
+    return int(code.value)
+
+
+def kernels_per_call() -> int:
+    return int(lib().gdn_kernels_per_call())

@@ -1,0 +1,189 @@
+// decode.cu -- single-token step of the gated delta-rule recurrence.
+//
+// The recurrence at S = 1 ("GDN Block TKG Kernel API Reference": the
+// single-token recurrence inside gdn_tkg, recurrent_state
+// [B, num_v_heads, head_k_dim, head_v_dim] fp32):
+//
+//     a  = exp(g);  p_k = S^T k;  p_q = S^T q
+//     d  = beta (v - a p_k)
+//     o  = scale S'^T q = scale (a p_q + d (k . q))
+//     S' = a S + k d^T                  (written back in place)
+//
+// The state dominates the traffic (64 KiB per head at Dk = Dv = 128), so the
+// kernel is built around one coalesced pass: every fp32 state element is loaded
+// once with a 128-bit load into registers, reduced, updated and stored once.
+//
+// Grid: (B * Hv, ceil(Dv / 64)).  A CTA owns one 64-column slice of one head's
+// state (columns evolve independently: column c of S' depends only on column c
+// of S).  128 threads = 16 column groups of 4 floats x 8 row groups; thread
+// (rg, cg) holds rows rg, rg + 8, ... of its 4 columns.  A warp therefore reads
+// two full 256-byte row segments per load instruction.
+#include <cuda_bf16.h>
+
+#include "gdn_internal.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kCols = 64;         // state columns per CTA
+constexpr int kThreads = 128;     // 16 column groups x 8 row groups
+constexpr int kRowGroups = 8;
+constexpr int kMaxRowsPerThread = 128 / kRowGroups;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
+
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) { return x; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
+
+template <typename T, bool kVec>
+__global__ void __launch_bounds__(kThreads) gdn_decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
+                                                              const T* __restrict__ v,
+                                                              const float* __restrict__ g_log,
+                                                              const float* __restrict__ beta, float scale,
+                                                              float* __restrict__ state, T* __restrict__ out,
+                                                              int Hk, int Hv, int Dk, int Dv, int zero_init) {
+    __shared__ float s_k[128];
+    __shared__ float s_q[128];
+    __shared__ float s_red[2][kRowGroups][kCols];
+    __shared__ float s_d[kCols];
+    __shared__ float s_kq;
+
+    const int bh = blockIdx.x;            // b * Hv + h
+    const int b = bh / Hv;
+    const int h = bh - b * Hv;
+    const int hk = h / (Hv / Hk);         // blocked GQA mapping
+    const int c_base = blockIdx.y * kCols;
+    const int tid = threadIdx.x;
+    const int cg = tid & 15;              // column group: 4 columns
+    const int rg = tid >> 4;              // row group
+    const int c0 = c_base + cg * 4;
+
+    const T* kp = k + (size_t)(b * Hk + hk) * Dk;
+    const T* qp = q + (size_t)(b * Hk + hk) * Dk;
+    float* Sp = state + (size_t)bh * Dk * Dv;
+
+    // Issue the state loads first: they are the bulk of the traffic.
+    float4 S[kMaxRowsPerThread];
+#pragma unroll
+    for (int i = 0; i < kMaxRowsPerThread; ++i) {
+        const int r = rg + i * kRowGroups;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!zero_init && r < Dk) {
+            if (kVec) {
+                if (c0 < Dv) x = __ldcs(reinterpret_cast<const float4*>(Sp + (size_t)r * Dv + c0));
+            } else {
+                const float* row = Sp + (size_t)r * Dv;
+                if (c0 + 0 < Dv) x.x = row[c0 + 0];
+                if (c0 + 1 < Dv) x.y = row[c0 + 1];
+                if (c0 + 2 < Dv) x.z = row[c0 + 2];
+                if (c0 + 3 < Dv) x.w = row[c0 + 3];
+            }
+        }
+        S[i] = x;
+    }
+
+    if (tid < Dk) {
+        s_k[tid] = to_f32(kp[tid]);
+        s_q[tid] = to_f32(qp[tid]);
+    }
+    const float a = expf(g_log[bh]);
+    const float bt = beta[bh];
+    __syncthreads();
+    if (tid < 32) {  // k . q
+        float acc = 0.f;
+        for (int i = tid; i < Dk; i += 32) acc += s_k[i] * s_q[i];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (tid == 0) s_kq = acc;
+    }
+
+    // Partial S^T k and S^T q over this thread's rows.
+    float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kMaxRowsPerThread; ++i) {
+        const int r = rg + i * kRowGroups;
+        if (r < Dk) {
+            const float kr = s_k[r], qr = s_q[r];
+            pk[0] += S[i].x * kr; pk[1] += S[i].y * kr; pk[2] += S[i].z * kr; pk[3] += S[i].w * kr;
+            pq[0] += S[i].x * qr; pq[1] += S[i].y * qr; pq[2] += S[i].z * qr; pq[3] += S[i].w * qr;
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        s_red[0][rg][cg * 4 + j] = pk[j];
+        s_red[1][rg][cg * 4 + j] = pq[j];
+    }
+    __syncthreads();
+    if (tid < kCols) {
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int g = 0; g < kRowGroups; ++g) {
+            sk += s_red[0][g][tid];
+            sq += s_red[1][g][tid];
+        }
+        const int c = c_base + tid;
+        const float vc = (c < Dv) ? to_f32(v[(size_t)bh * Dv + c]) : 0.f;
+        const float d = bt * (vc - a * sk);
+        s_d[tid] = d;
+        if (c < Dv) out[(size_t)bh * Dv + c] = from_f32<T>(scale * (a * sq + d * s_kq));
+    }
+    __syncthreads();
+
+    const float d0 = s_d[cg * 4 + 0], d1 = s_d[cg * 4 + 1], d2 = s_d[cg * 4 + 2], d3 = s_d[cg * 4 + 3];
+#pragma unroll
+    for (int i = 0; i < kMaxRowsPerThread; ++i) {
+        const int r = rg + i * kRowGroups;
+        if (r < Dk) {
+            const float kr = s_k[r];
+            float4 x;
+            x.x = a * S[i].x + kr * d0;
+            x.y = a * S[i].y + kr * d1;
+            x.z = a * S[i].z + kr * d2;
+            x.w = a * S[i].w + kr * d3;
+            if (kVec) {
+                if (c0 < Dv) __stcs(reinterpret_cast<float4*>(Sp + (size_t)r * Dv + c0), x);
+            } else {
+                float* row = Sp + (size_t)r * Dv;
+                if (c0 + 0 < Dv) row[c0 + 0] = x.x;
+                if (c0 + 1 < Dv) row[c0 + 1] = x.y;
+                if (c0 + 2 < Dv) row[c0 + 2] = x.z;
+                if (c0 + 3 < Dv) row[c0 + 3] = x.w;
+            }
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_typed(const Problem& p, cudaStream_t stream) {
+    dim3 grid(p.B * p.Hv, (p.Dv + kCols - 1) / kCols);
+    const bool vec = (p.Dv % 4) == 0;
+    const T* q = static_cast<const T*>(p.q);
+    const T* k = static_cast<const T*>(p.k);
+    const T* v = static_cast<const T*>(p.v);
+    T* out = static_cast<T*>(p.out);
+    if (vec)
+        gdn_decode_kernel<T, true><<<grid, kThreads, 0, stream>>>(q, k, v, p.g_log, p.beta, p.scale, p.state, out,
+                                                                  p.Hk, p.Hv, p.Dk, p.Dv, p.zero_init ? 1 : 0);
+    else
+        gdn_decode_kernel<T, false><<<grid, kThreads, 0, stream>>>(q, k, v, p.g_log, p.beta, p.scale, p.state,
+                                                                   out, p.Hk, p.Hv, p.Dk, p.Dv,
+                                                                   p.zero_init ? 1 : 0);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_decode(const Problem& p, cudaStream_t stream) {
+    return p.bf16 ? launch_typed<__nv_bfloat16>(p, stream) : launch_typed<float>(p, stream);
+}
+
+}  // namespace gdn

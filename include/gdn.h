@@ -1,0 +1,144 @@
+/*
+ * gdn.h -- C ABI of the gated delta-rule (GDN) library for NVIDIA GB300 (sm_103a).
+ *
+ * The library computes the gated delta-rule linear-attention recurrence named
+ * in the "Background" section of the "GDN CTE Kernel API Reference" page:
+ * for every batch b, value head h (reading query/key head h / (Hv/Hk)) and
+ * token t,
+ *
+ *     S_t = exp(g_t) S_{t-1} + beta_t k_t (v_t - exp(g_t) S_{t-1}^T k_t)^T
+ *     o_t = scale * S_t^T q_t
+ *
+ * with an fp32 state S of shape [Dk, Dv].  Two entry points compute it:
+ * a chunk-parallel prefill over a whole sequence (gdn_prefill) and one
+ * single-token step (gdn_decode_step).
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers to contiguous row-major memory
+ *     owned by the caller; the library never allocates, frees or keeps them.
+ *   - Work is enqueued on `stream`; calls return before the GPU finishes.
+ *     Host-side argument checks run first: when one fails, nothing is launched
+ *     and the error code is returned.  Asynchronous kernel faults surface at
+ *     the caller's next synchronisation; kernel-side wait timeouts are recorded
+ *     in a per-device status word read by gdn_device_status().
+ *   - Preconditions the library does NOT check: q and k are L2-normalised per
+ *     token ("GDN CTE Kernel API Reference", Notes), g_log <= 0 (Parameters /
+ *     g_log), beta in (0, 1) (Parameters / beta), and the buffers do not overlap
+ *     except state_inout with itself.
+ */
+#ifndef GDN_H
+#define GDN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Same handle as cudaStream_t / CUstream; NULL is the legacy default stream. */
+typedef struct CUstream_st* gdn_stream_t;
+
+typedef enum {
+    GDN_OK = 0,
+    GDN_ERR_NULL = 1,        /* a required pointer is NULL                                  */
+    GDN_ERR_DIMS = 2,        /* dims inconsistent with the pages' constraints (see gdn_dims) */
+    GDN_ERR_UNSUPPORTED = 3, /* allowed by the pages but not implemented by this build      */
+    GDN_ERR_ALIGN = 4,       /* a tensor pointer is not 16-byte aligned                     */
+    GDN_ERR_CUDA = 5,        /* a CUDA call (launch, attribute, tensor-map encode) failed    */
+    GDN_ERR_TIMEOUT = 6      /* a kernel wait ran past its bound (device status only)        */
+} gdn_status;
+
+/* Compute dtype = dtype of q, k, v and out ("GDN CTE Kernel API Reference",
+ * Parameters / query: the query's dtype sets the compute dtype).  g_log, beta
+ * and the state are always fp32. */
+typedef enum { GDN_F32 = 0, GDN_BF16 = 1 } gdn_dtype;
+
+enum {
+    /* The "omitted" recurrent_state form (Parameters / recurrent_state): start
+     * from a zero state and emit no load.  state_inout is still required and
+     * receives the final state. */
+    GDN_ZERO_INITIAL_STATE = 1u << 0,
+    /* Run the prefill on the fp32 FFMA kernel even where the tensor-core kernel
+     * applies (a cross-check path; same results within fp32 rounding). */
+    GDN_FORCE_FFMA = 1u << 1
+};
+
+/*
+ * Problem sizes ("GDN CTE Kernel API Reference", Dimensions and Notes):
+ *   B  >= 0 batch (0: nothing to do);  Hk >= 1 key/query heads;
+ *   Hv >= 1 value heads with Hv % Hk == 0;
+ *   S  >= 0 tokens for the prefill (0: no tokens, the state is left as it is,
+ *      or zeroed under GDN_ZERO_INITIAL_STATE); the decode step requires S == 1;
+ *   Dk, Dv in [1, 128] head dims (Dq == Dk: q and k share Dk).
+ * Violations return GDN_ERR_DIMS.  The pages' S % 128 rule belongs to their
+ * Trainium algorithm choice; this library accepts any S.  When B == 0 or
+ * S == 0, q, k, v, g_log, beta and out may be NULL.
+ */
+typedef struct {
+    int64_t B, Hk, Hv, S, Dk, Dv;
+    int32_t dtype;   /* gdn_dtype */
+    uint32_t flags;  /* GDN_ZERO_INITIAL_STATE | GDN_FORCE_FFMA */
+} gdn_dims;
+
+/*
+ * gdn_prefill -- chunk-parallel prefill of the recurrence over S tokens.
+ * ("GDN CTE Kernel API Reference", API Reference / gdn_cte: Parameters, Returns.)
+ *
+ *   q           [B, Hk, S, Dk]  compute dtype, token-major, L2-normalised rows
+ *   k           [B, Hk, S, Dk]  compute dtype, token-major, L2-normalised rows
+ *   v           [B, Hv, S, Dv]  compute dtype
+ *   g_log       [B, Hv, S]      fp32 per-token log-decay (negative)
+ *   beta        [B, Hv, S]      fp32 per-token update strength in (0, 1)
+ *   scale       query scale, applied on the device (typically 1/sqrt(Dk))
+ *   state_inout [B, Hv, Dk, Dv] fp32, Dv contiguous.  Read as the initial state
+ *               (unless GDN_ZERO_INITIAL_STATE) and overwritten in place with the
+ *               final state (the page's aliased in/out recurrent_state).
+ *   out         [B, Hv, S, Dv]  compute dtype, head-major, un-normalised
+ *
+ * Every pointer must be non-NULL and 16-byte aligned.  Returns GDN_OK once the
+ * work is enqueued.  Implementation: Dk = Dv = 128 with bf16 runs on the
+ * tcgen05 tensor-core kernel; every other supported shape and fp32 compute run
+ * on the FFMA kernel.
+ */
+gdn_status gdn_prefill(const void* q, const void* k, const void* v,
+                       const float* g_log, const float* beta, float scale,
+                       float* state_inout, void* out,
+                       const gdn_dims* dims, gdn_stream_t stream);
+
+/*
+ * gdn_decode_step -- one token of the recurrence (the prefill at S = 1), the
+ * core of the single-token step of the "GDN Block TKG Kernel API Reference"
+ * page (its recurrent_state [B, num_v_heads, head_k_dim, head_v_dim] fp32).
+ * Same arguments and layouts as gdn_prefill with dims->S == 1 (else
+ * GDN_ERR_DIMS).  The state is updated in place: each fp32 state element is
+ * read once and written once.
+ */
+gdn_status gdn_decode_step(const void* q, const void* k, const void* v,
+                           const float* g_log, const float* beta, float scale,
+                           float* state_inout, void* out,
+                           const gdn_dims* dims, gdn_stream_t stream);
+
+/* Device workspace gdn_prefill needs for these dims: always 0 (every kernel
+ * keeps its intermediates on chip). */
+size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);
+
+/* Static, NUL-terminated description of a status code. */
+const char* gdn_status_string(gdn_status s);
+
+/*
+ * gdn_device_status -- read (and, when clear != 0, reset to 0) the kernel-side
+ * status word of CUDA device `device`.  0 means no kernel reported a problem;
+ * otherwise the value is a gdn_status (GDN_ERR_TIMEOUT).  Synchronises the
+ * device.  Returns GDN_ERR_NULL if code is NULL, GDN_ERR_CUDA if the copy fails.
+ */
+gdn_status gdn_device_status(int device, int clear, int32_t* code);
+
+/* Number of kernels one call launches (both entry points launch exactly one). */
+int gdn_kernels_per_call(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* GDN_H */

@@ -1,0 +1,100 @@
+"""The C-ABI library loads, exports every symbol include/gdn.h declares, and its
+host-side argument checks reject bad calls before any launch.  No call here
+reaches a kernel, so this file runs without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import gated_delta_rule_20_gb300 as gdn
+from gated_delta_rule_20_gb300 import build as gbuild
+
+HEADER = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "gdn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    gbuild.build()
+    return gdn.lib()
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?[a-z_0-9]+\s*\*?\s*(gdn_[a-z_0-9]+)\s*\(", src, flags=re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert "gdn_prefill" in names and "gdn_decode_step" in names
+    assert set(names) == set(gdn.EXPORTED)
+
+
+def test_library_exports_every_declared_symbol(L):
+    for name in declared_functions():
+        assert hasattr(L, name), name
+
+
+def test_status_strings(L):
+    for code in range(7):
+        s = gdn.status_string(code)
+        assert s.startswith("GDN_"), s
+    assert "unknown" in gdn.status_string(99)
+
+
+def test_workspace_is_zero(L):
+    d = gdn.make_dims(4, 16, 32, 4096, 128, 128, gdn.GDN_BF16)
+    assert L.gdn_prefill_workspace_bytes(ctypes.byref(d)) == 0
+    assert gdn.kernels_per_call() == 1
+
+
+def _call(L, name, dims, ptr=16, state=16):
+    p = ctypes.c_void_p(ptr) if ptr is not None else None
+    s = ctypes.c_void_p(state) if state is not None else None
+    return getattr(L, name)(p, p, p, p, p, ctypes.c_float(1.0), s, p,
+                            ctypes.byref(dims) if dims is not None else None, None)
+
+
+@pytest.mark.parametrize("name", ["gdn_prefill", "gdn_decode_step"])
+def test_argument_checks(L, name):
+    S = 1 if name == "gdn_decode_step" else 64
+    ok = dict(B=2, Hk=2, Hv=4, S=S, Dk=128, Dv=128, dtype=gdn.GDN_BF16)
+
+    def dims(**kw):
+        a = dict(ok)
+        a.update(kw)
+        return gdn.make_dims(a["B"], a["Hk"], a["Hv"], a["S"], a["Dk"], a["Dv"], a["dtype"], a.get("flags", 0))
+
+    assert _call(L, name, None) == gdn.GDN_ERR_NULL
+    assert _call(L, name, dims(), ptr=None) == gdn.GDN_ERR_NULL
+    assert _call(L, name, dims(), state=None) == gdn.GDN_ERR_NULL
+    assert _call(L, name, dims(Hv=3)) == gdn.GDN_ERR_DIMS          # Hv % Hk != 0
+    assert _call(L, name, dims(Dk=129)) == gdn.GDN_ERR_DIMS        # > MAX_HEAD_DIM
+    assert _call(L, name, dims(Dv=129)) == gdn.GDN_ERR_DIMS
+    assert _call(L, name, dims(Dk=0)) == gdn.GDN_ERR_DIMS
+    assert _call(L, name, dims(Hk=0)) == gdn.GDN_ERR_DIMS
+    assert _call(L, name, dims(B=-1)) == gdn.GDN_ERR_DIMS
+    assert _call(L, name, dims(S=-1)) == gdn.GDN_ERR_DIMS
+    assert _call(L, name, dims(dtype=7)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _call(L, name, dims(flags=1 << 9)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _call(L, name, dims(), ptr=24) == gdn.GDN_ERR_ALIGN       # not 16-byte aligned
+    assert _call(L, name, dims(), state=8) == gdn.GDN_ERR_ALIGN
+    if name == "gdn_decode_step":
+        assert _call(L, name, dims(S=2)) == gdn.GDN_ERR_DIMS
+
+
+def test_empty_batch_is_a_no_op(L):
+    # B = 0: nothing to compute, no CUDA call is made.
+    d = gdn.make_dims(0, 2, 4, 64, 128, 128, gdn.GDN_BF16)
+    assert _call(L, "gdn_prefill", d) == gdn.GDN_OK
+    d = gdn.make_dims(0, 2, 4, 1, 128, 128, gdn.GDN_BF16)
+    assert _call(L, "gdn_decode_step", d) == gdn.GDN_OK
+
+
+def test_binding_requires_cuda_tensors():
+    torch = pytest.importorskip("torch")
+    q = torch.zeros(1, 1, 4, 8)
+    with pytest.raises(ValueError):
+        gdn.prefill(q, q, q, torch.zeros(1, 1, 4), torch.zeros(1, 1, 4), 1.0, torch.zeros(1, 1, 8, 8),
+                    torch.zeros(1, 1, 4, 8))
