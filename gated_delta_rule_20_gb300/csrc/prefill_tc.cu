@@ -12,35 +12,46 @@
 // log-decay inside the chunk, gamma_r = exp(G_r):
 //     A[r][j] = beta_r exp(G_r - G_j) k_r.k_j  (j < r)        T = (I + A)^-1
 //     U = T diag(beta) V,  W = T diag(beta gamma) K,  Delta = U - W S0
-//     O = scale (diag(gamma) Q S0 + P Delta),  P[r][j] = exp(G_r - G_j) q_r.k_j (j <= r)
-//     S_end = gamma_C S0 + sum_j exp(G_C - G_j) k_j Delta_j^T
+//     O = scale (Q' S0 + P Delta),  Q' = diag(gamma) Q,
+//         P[r][j] = exp(G_r - G_j) q_r.k_j (j <= r)
+//     S_end = gamma_C S0 + K~^T Delta,  K~ = diag(exp(G_C - G)) K
 // Only exponents <= 0 are ever evaluated, so strong decay cannot overflow.
 //
 // Orientation.  Every tensor-core product is issued with M = 128 by putting a
 // head dimension (Dv or Dk = 128) on the M / TMEM-lane axis and the chunk's 64
 // tokens on N:
-//     R_KQ  = [K; Q] K^T          (lanes 0..63: K K^T rows, 64..127: Q K^T rows)
-//     R_QS  = S0^T Q^T            (lanes = dv, columns = token r)
-//     R_U   = V^T (T diag beta)^T               -> U^T
-//     R_W   = K^T (T diag beta gamma)^T         -> W^T
-//     R_U  += S0^T (-W)^T                       -> Delta^T
-//     R_PD  = Delta^T P^T                       (reuses R_KQ's columns)
-//     R_SN  = (Delta diag(exp(G_C - G)))^T K    -> increment of S^T
-// The fp32 state lives in TMEM as S^T (lane = dv, column = dk); a bf16 copy in
-// shared memory is the A operand of the two products that read S0.
-// Thread i of the 128-thread CTA owns TMEM lane i (dv row i, or dk row i, or
-// token row i of the Gram products), so every epilogue step is row-local.
+//     R_G    = [K; Q] K^T       (lanes 0..63: K K^T rows, 64..127: Q K^T rows)
+//     R_U[s] = V^T (T diag beta)^T               -> U^T
+//     R_W    = K^T (T diag beta gamma)^T         -> W^T
+//     R_U[s] += S0^T (-W)^T                      -> Delta^T   (chain)
+//     R_O[s] = S0^T Q'^T + Delta^T P^T           -> O^T / scale (chain)
+//     R_S   += Delta^T K~                        -> state increment, S^T layout
 //
-// Structure: one CTA per (batch, value head); one thread issues TMA loads and
-// MMAs; the chunk inputs (q, k, v tiles) are double-buffered so the next
-// chunk's loads overlap this chunk's work.  Every wait is bounded; a wait that
-// gives up records GDN_ERR_TIMEOUT in the device status word, drains what is in
-// flight (again bounded), frees TMEM and returns.
+// Roles (one CTA per (batch, value head), 384 threads):
+//   prep warps (0-7)  -- per chunk: decay scan, the Gram product, A and P,
+//       the triangular solve, U and W, and the in-place rewrites Q -> Q',
+//       V -> -W, K -> K~ inside the chunk's input stage.  Warp w reads TMEM
+//       lanes 32 (w % 4) .. + 31 and, for 64-column products, columns
+//       32 (w / 4) .. + 31.  Prep runs up to one chunk ahead of the chain.
+//   chain warps (8-11) -- the serial part: Delta, the state carry (fp32 S^T in
+//       TMEM, lane i = dv row i, scaled by gamma_C in place and incremented
+//       by the tensor core), the output and its TMA store.  Once the products
+//       of chunk c have completed, the chain reloads that chunk's input stage
+//       with chunk c + 2 (TMA) and prefetches chunk c + 3 into L2.
+//
+// Triangular solve: (I + A)^-1 for the 64x64 strictly lower A, blocked in
+// 16x16: diagonal blocks by forward substitution in fp32, off-diagonal blocks
+// by block elimination T_ij = -T_ii (A_ij T_jj) (level 1: inside each 32x32
+// half; level 2: the lower-left 32x32 block) on warp-level tf32 MMAs with fp32
+// accumulation.
+//
+// Every wait is bounded; a wait that gives up records GDN_ERR_TIMEOUT in the
+// device status word, makes the other roles give up too, drains what it has
+// in flight (bounded), and the CTA frees its TMEM and returns.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
-#include <cstdio>
 #include <mutex>
 
 #include "gdn_internal.h"
@@ -51,56 +62,62 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kC = 64;        // tokens per chunk
-constexpr int kD = 128;       // Dk = Dv
-constexpr int kThreads = 128;
+constexpr int kC = 64;   // tokens per chunk
+constexpr int kD = 128;  // Dk = Dv
+constexpr int kPrep = 256;
+constexpr int kChain = 128;
+constexpr int kThreads = kPrep + kChain;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns (fp32, 128 lanes each)
-constexpr uint32_t COL_KQ = 0;    // 64: [K;Q] K^T, later Delta^T P^T
-constexpr uint32_t COL_U = 64;    // 64: U^T, then Delta^T
-constexpr uint32_t COL_W = 128;   // 64: W^T
-constexpr uint32_t COL_QS = 192;  // 64: S0^T Q^T
-constexpr uint32_t COL_SN = 256;  // 128: state increment (S^T layout)
-constexpr uint32_t COL_S = 384;   // 128: fp32 state S^T
+constexpr uint32_t COL_G = 0;    // 64: Gram
+constexpr uint32_t COL_U = 64;   // 2 x 64: U^T then Delta^T, per stage
+constexpr uint32_t COL_W = 192;  // 64: W^T
+constexpr uint32_t COL_O = 256;  // 2 x 64: output accumulators, per stage
+constexpr uint32_t COL_S = 384;  // 128: the fp32 state S^T (lane dv, column dk)
 
-// Shared memory (bytes from a 1024-aligned base).  All bf16 tiles use rows of
-// 128 bytes with the 128-byte swizzle.
-constexpr uint32_t STAGE_BYTES = 49152;
-constexpr uint32_t ST_K0 = 0;       // K, dk 0..63   [64 tokens][64]
-constexpr uint32_t ST_Q0 = 8192;    // Q, dk 0..63
-constexpr uint32_t ST_K1 = 16384;   // K, dk 64..127
-constexpr uint32_t ST_Q1 = 24576;   // Q, dk 64..127
-constexpr uint32_t ST_V0 = 32768;   // V, dv 0..63
-constexpr uint32_t ST_V1 = 40960;   // V, dv 64..127
-constexpr uint32_t OFF_T1 = 2 * STAGE_BYTES;  // T diag(beta)        [64 r][64 j] K-major
-constexpr uint32_t OFF_T2 = OFF_T1 + 8192;    // T diag(beta gamma)  [64 r][64 j]
-constexpr uint32_t OFF_P = OFF_T2 + 8192;     // P                   [64 r][64 j]
-constexpr uint32_t OFF_WD = OFF_P + 8192;     // -W as [dk][64 r] (MN-major B), then Delta^T [dv][64 j]
-constexpr uint32_t OFF_DT = OFF_WD + 16384;   // Delta~^T [dv][64 j]; fp32 T during the solve
-constexpr uint32_t OFF_SB = OFF_DT + 16384;   // S^T bf16 [dv][dk]: dk halves at +0, +16384
-constexpr uint32_t OFF_OUT = OFF_SB + 32768;  // out tile: dv halves at +0, +8192; fp32 A during the solve
-constexpr uint32_t OFF_SMALL = OFF_OUT + 16384;  // G, gamma, beta, exp(G_C - G): 4 x 64 floats
-constexpr uint32_t OFF_BAR = OFF_SMALL + 1024;   // 3 mbarriers, TMEM base, flags
-constexpr uint32_t SMEM_USED = OFF_BAR + 64;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;  // slack for the 1024-byte alignment
-
+// Shared memory (bytes from a 1024-aligned base).  bf16 tiles: rows of 128 B
+// with the 128-byte swizzle.
+constexpr uint32_t STAGE_BYTES = 57344;
+constexpr uint32_t ST_K0 = 0;      // K (-> K~), dk 0..63     [64 tokens][64]
+constexpr uint32_t ST_Q0 = 8192;   // Q (-> Q'), dk 0..63
+constexpr uint32_t ST_K1 = 16384;  // K (-> K~), dk 64..127
+constexpr uint32_t ST_Q1 = 24576;  // Q (-> Q'), dk 64..127
+constexpr uint32_t ST_V = 32768;   // V as two [64][64] boxes; then -W as [128 dk][64 r]
+constexpr uint32_t ST_P = 49152;   // P [64 r][64 j]
+constexpr uint32_t LOAD_BYTES = 49152;
+constexpr uint32_t OFF_T12 = 2 * STAGE_BYTES;  // T diag(beta), T diag(beta gamma): [64 r][64 j] bf16 each
+constexpr uint32_t OFF_AT = OFF_T12 + 16384;   // fp32 A, solved in place into T: [64][68]
+constexpr int AT_STRIDE = 68;
+constexpr uint32_t OFF_SB = OFF_AT + 17408;    // S^T bf16 [dv][dk]: dk halves at +0, +16384
+constexpr uint32_t OFF_DT = OFF_SB + 32768;    // Delta^T bf16 [dv][64 j]
+constexpr uint32_t OFF_OUT = OFF_DT + 16384;   // out tile [64 r][128 dv] bf16, unswizzled
+constexpr uint32_t OFF_SCR = OFF_OUT + 16384;   // solve scratch (fp32 X tiles)
+constexpr uint32_t OFF_SMALL = OFF_SCR + 8192;
+// small area (floats): G2[64] = log2(e) x cumulative log-decay, gam[64], bet[64],
+// ec[2][64] (per stage: read late in the chunk), gC[2]
+constexpr uint32_t OFF_BAR = OFF_SMALL + 1536;
+constexpr uint32_t SMEM_USED = OFF_BAR + 128;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
+static_assert(OFF_SB % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_OUT % 1024 == 0, "tile alignment");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
+// solve scratch
+constexpr uint32_t SCR_X1 = 0;     // level 1: 4 tiles of 16 x 8 fp32 (stride 8)
+constexpr uint32_t SCR_X2 = 2048;  // level 2: 32 x 32 fp32 (stride 40)
+constexpr int X2_STRIDE = 40;
 
-// Instruction descriptors (M = 128 always).
 constexpr uint32_t IDESC_N64_KK = make_idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t IDESC_N64_MK = make_idesc_bf16(128, 64, 1, 0);   // A MN-major
 constexpr uint32_t IDESC_N64_KM = make_idesc_bf16(128, 64, 0, 1);   // B MN-major
 constexpr uint32_t IDESC_N128_KM = make_idesc_bf16(128, 128, 0, 1);
 
-// fp32 64x64 scratch with an XOR swizzle on the column: conflict-free row and
-// column access.
-__device__ __forceinline__ int fidx(int r, int c) { return r * 64 + (c ^ (r & 31)); }
+constexpr uint32_t BAR_PREP = 1;   // named barrier: the 8 prep warps
+constexpr uint32_t BAR_CHAIN = 2;  // named barrier: the 4 chain warps
+constexpr uint32_t BAR_SCAN = 3;   // prep warps 0, 1 (the decay scan)
+constexpr uint32_t BAR_L1 = 4;     // prep warps 0..3 (level 1 of the solve)
 
-// Write 32 fp32 values as bf16 into a 128-byte-swizzled row: bytes
-// [byte0, byte0 + 64) of row `row` of the tile at `tile`.
-__device__ __forceinline__ void st_row_bf16x32(uint8_t* tile, int row, int byte0, const float (&x)[32],
-                                               float mul = 1.0f) {
+// bf16 row writer: 32 fp32 values -> bytes [byte0, byte0 + 64) of a swizzled row.
+__device__ __forceinline__ void st_row_bf16x32(uint8_t* tile, int row, int byte0, const float* x, float mul = 1.f) {
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
         uint4 w;
@@ -112,139 +129,145 @@ __device__ __forceinline__ void st_row_bf16x32(uint8_t* tile, int row, int byte0
     }
 }
 
-struct Shared {
-    uint8_t* base;
-    uint32_t sbase;
-    float* G;
-    float* gam;
-    float* bet;
-    float* ec;
-    uint64_t* bar_tma;  // [2]
-    uint64_t* bar_mma;
-    uint32_t* tmem_slot;
+// Scale `n` 16-byte chunks (8 bf16 each) of one 128-byte row by s, in place,
+// starting at chunk `q0`; the visiting order is rotated by the row so threads
+// on neighbouring rows hit different banks.
+template <int N>
+__device__ __forceinline__ void scale_row_chunks(uint8_t* tile, int row, int q0, float s) {
+    const Bf16Scale sc = make_bf16_scale(s);
+    uint4* p = reinterpret_cast<uint4*>(tile + row * 128);
+#pragma unroll
+    for (int i = 0; i < N; ++i) {
+        const int q = q0 + ((i + row) & (N - 1));
+        uint4 w = p[q];
+        w.x = scale_bf16x2(w.x, sc);
+        w.y = scale_bf16x2(w.y, sc);
+        w.z = scale_bf16x2(w.z, sc);
+        w.w = scale_bf16x2(w.w, sc);
+        p[q] = w;
+    }
+}
+
+// Output: thread ct holds column dv = ct of O^T / scale in TMEM (64 tokens);
+// write scale * O into the unswizzled [64 tokens][128 dv] bf16 staging tile.
+__device__ __forceinline__ void write_out_tile(uint8_t* tile, uint32_t taddr, int ct, float scale) {
+    float x0[32], x1[32];
+    tmem_ld32(taddr, x0);
+    tmem_ld32(taddr + 32, x1);
+    tmem_wait_ld();
+    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(tile) + ct;
+#pragma unroll
+    for (int r = 0; r < 32; ++r) {
+        ob[r * kD] = __float2bfloat16_rn(scale * x0[r]);
+        ob[(r + 32) * kD] = __float2bfloat16_rn(scale * x1[r]);
+    }
+}
+
+struct Bars {
+    uint64_t full[2];   // TMA -> prep
+    uint64_t ready[2];  // prep -> chain (kPrep arrivals)
+    uint64_t prep_mma;  // prep's MMA commits
+    uint64_t c1;        // chain: Delta product done
+    uint64_t c2;        // chain: state increment done
+    uint64_t c3;        // chain: output accumulator done
+    uint32_t tmem_base;
+    int abort;
 };
 
-__device__ __forceinline__ void issue_chunk_loads(const Shared& sh, int stage, const CUtensorMap* tq,
-                                                  const CUtensorMap* tk, const CUtensorMap* tv, int t0, int bhk,
-                                                  int bh) {
-    uint8_t* st = sh.base + stage * STAGE_BYTES;
-    uint64_t* bar = &sh.bar_tma[stage];
-    mbar_arrive_expect_tx(bar, STAGE_BYTES);
+// ---------------------------------------------------------------- solve
+// Warp-level tf32 fragments (m16n8k8) of fp32 matrices in shared memory.
+__device__ __forceinline__ void load_afrag(const float* M, int ld, int r0, int k0, int g, int t, uint32_t (&a)[4]) {
+    a[0] = f32_to_tf32(M[(r0 + g) * ld + k0 + t]);
+    a[1] = f32_to_tf32(M[(r0 + g + 8) * ld + k0 + t]);
+    a[2] = f32_to_tf32(M[(r0 + g) * ld + k0 + t + 4]);
+    a[3] = f32_to_tf32(M[(r0 + g + 8) * ld + k0 + t + 4]);
+}
+__device__ __forceinline__ void load_bfrag(const float* M, int ld, int k0, int n0, int g, int t, uint32_t (&b)[2]) {
+    b[0] = f32_to_tf32(M[(k0 + t) * ld + n0 + g]);
+    b[1] = f32_to_tf32(M[(k0 + t + 4) * ld + n0 + g]);
+}
+__device__ __forceinline__ void store_cfrag(float* M, int ld, int r0, int n0, int g, int t, const float (&d)[4],
+                                            float s) {
+    *reinterpret_cast<float2*>(&M[(r0 + g) * ld + n0 + 2 * t]) = make_float2(s * d[0], s * d[1]);
+    *reinterpret_cast<float2*>(&M[(r0 + g + 8) * ld + n0 + 2 * t]) = make_float2(s * d[2], s * d[3]);
+}
+
+// Write the 16 x 8 tile (r0.., n0..) of T held as a C fragment (scaled by s)
+// straight into the bf16 tiles T diag(beta) and T diag(beta gamma).
+__device__ __forceinline__ void store_t12_frag(uint8_t* t12, const float* bet, const float* gam, int r0, int n0,
+                                               int g, int t, const float (&d)[4], float s) {
+    const int j = n0 + 2 * t;
+    const float b0 = bet[j] * s, b1 = bet[j + 1] * s;
+    const float c0 = b0 * gam[j], c1 = b1 * gam[j + 1];
+    const uint32_t o0 = sw128_offset(r0 + g, 2 * j), o1 = sw128_offset(r0 + g + 8, 2 * j);
+    *reinterpret_cast<uint32_t*>(t12 + o0) = pack_bf16x2(d[0] * b0, d[1] * b1);
+    *reinterpret_cast<uint32_t*>(t12 + o1) = pack_bf16x2(d[2] * b0, d[3] * b1);
+    *reinterpret_cast<uint32_t*>(t12 + 8192 + o0) = pack_bf16x2(d[0] * c0, d[1] * c1);
+    *reinterpret_cast<uint32_t*>(t12 + 8192 + o1) = pack_bf16x2(d[2] * c0, d[3] * c1);
+}
+
+// Level 0: diagonal 16 x 16 block `blk` of T = (I + A)^-1 by forward
+// substitution, one column per lane (lanes 16..31 repeat lanes 0..15).
+__device__ __forceinline__ void solve_diag_block(float* M, int blk, int lane) {
+    const int base = blk * 16, j = lane & 15;
+    float x[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const float* row = M + (base + i) * AT_STRIDE + base;
+        float acc = (i == j) ? 1.f : 0.f;
+#pragma unroll
+        for (int m = 0; m < i; ++m) acc = fmaf(-row[m], x[m], acc);
+        x[i] = acc;
+    }
+    __syncwarp();
+    if (lane < 16) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) M[(base + i) * AT_STRIDE + base + j] = x[i];
+    }
+}
+
+// ---------------------------------------------------------------- TMA
+__device__ __forceinline__ void load_chunk(uint8_t* st, uint64_t* bar, const CUtensorMap* tq, const CUtensorMap* tk,
+                                           const CUtensorMap* tv, int c, int bhk, int bh) {
+    const int t0 = c * kC;
+    mbar_arrive_expect_tx(bar, LOAD_BYTES);
     tma_load_3d(st + ST_K0, tk, bar, 0, t0, bhk);
     tma_load_3d(st + ST_Q0, tq, bar, 0, t0, bhk);
     tma_load_3d(st + ST_K1, tk, bar, 64, t0, bhk);
     tma_load_3d(st + ST_Q1, tq, bar, 64, t0, bhk);
-    tma_load_3d(st + ST_V0, tv, bar, 0, t0, bh);
-    tma_load_3d(st + ST_V1, tv, bar, 64, t0, bh);
+    tma_load_3d(st + ST_V, tv, bar, 0, t0, bh);
+    tma_load_3d(st + ST_V + 8192, tv, bar, 64, t0, bh);
+}
+__device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
+                                                  int c, int bhk, int bh) {
+    const int t0 = c * kC;
+    tma_prefetch_l2_3d(tk, 0, t0, bhk);
+    tma_prefetch_l2_3d(tk, 64, t0, bhk);
+    tma_prefetch_l2_3d(tq, 0, t0, bhk);
+    tma_prefetch_l2_3d(tq, 64, t0, bhk);
+    tma_prefetch_l2_3d(tv, 0, t0, bh);
+    tma_prefetch_l2_3d(tv, 64, t0, bh);
 }
 
-// T = (I + A)^-1 for a strictly lower 64x64 A (fp32, fidx layout), blocked in
-// 16x16: diagonal blocks by forward substitution, then the off-diagonal
-// blocks by block elimination  T_ij = -T_ii (sum_k A_ik T_kj)  in two levels.
-__device__ __forceinline__ void solve_unit_lower_64(const float* A, float* T, int tid) {
-    // Level 0: the four diagonal 16x16 blocks; the upper blocks are zeroed.
-    if (tid < 64) {
-        const int base = (tid >> 4) * 16, jj = tid & 15;
-        float x[16];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            float acc = (i == jj) ? 1.f : 0.f;
-#pragma unroll
-            for (int m = 0; m < i; ++m) acc -= A[fidx(base + i, base + m)] * x[m];
-            x[i] = acc;
-        }
-#pragma unroll
-        for (int i = 0; i < 16; ++i) T[fidx(base + i, base + jj)] = x[i];
-    } else {
-        for (int e = tid - 64; e < 6 * 256; e += 64) {
-            const int blk = e >> 8, w = e & 255;
-            // upper blocks (bi, bj), bi < bj: (0,1) (0,2) (0,3) (1,2) (1,3) (2,3)
-            const int bi = blk < 3 ? 0 : (blk < 5 ? 1 : 2);
-            const int bj = blk < 3 ? blk + 1 : (blk < 5 ? blk - 1 : 3);
-            T[fidx(bi * 16 + (w >> 4), bj * 16 + (w & 15))] = 0.f;
-        }
-    }
-    __syncthreads();
-    // Level 1: blocks (1,0), (2,1), (3,2).  96 threads: 16 rows x 2 column halves per block.
-    float y[8];
-    const bool l1 = tid < 96;
-    const int blk = tid >> 5, r16 = tid & 15, c8 = ((tid >> 4) & 1) * 8;
-    if (l1) {
-        const int rb = 16 * (blk + 1), cb = 16 * blk;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) y[u] = 0.f;
-#pragma unroll 4
-        for (int m = 0; m < 16; ++m) {
-            const float a = A[fidx(rb + r16, cb + m)];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) y[u] += a * T[fidx(cb + m, cb + c8 + u)];
-        }
-#pragma unroll
-        for (int u = 0; u < 8; ++u) T[fidx(rb + r16, cb + c8 + u)] = y[u];  // X = A_(b+1,b) T_bb
-    }
-    __syncthreads();
-    if (l1) {
-        const int rb = 16 * (blk + 1), cb = 16 * blk;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) y[u] = 0.f;
-#pragma unroll 4
-        for (int m = 0; m < 16; ++m) {
-            const float t = T[fidx(rb + r16, rb + m)];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) y[u] -= t * T[fidx(rb + m, cb + c8 + u)];
-        }
-    }
-    __syncthreads();
-    if (l1) {
-        const int rb = 16 * (blk + 1), cb = 16 * blk;
-#pragma unroll
-        for (int u = 0; u < 8; ++u) T[fidx(rb + r16, cb + c8 + u)] = y[u];
-    }
-    __syncthreads();
-    // Level 2: block rows 32..63 x cols 0..31.  Thread: row 32 + (tid & 31), 8 columns.
-    const int r32 = tid & 31, c32 = (tid >> 5) * 8;
-#pragma unroll
-    for (int u = 0; u < 8; ++u) y[u] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < 32; ++m) {
-        const float a = A[fidx(32 + r32, m)];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) y[u] += a * T[fidx(m, c32 + u)];
-    }
-#pragma unroll
-    for (int u = 0; u < 8; ++u) T[fidx(32 + r32, c32 + u)] = y[u];
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 8; ++u) y[u] = 0.f;
-#pragma unroll 4
-    for (int m = 0; m < 32; ++m) {
-        const float t = T[fidx(32 + r32, 32 + m)];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) y[u] -= t * T[fidx(32 + m, c32 + u)];
-    }
-    __syncthreads();
-#pragma unroll
-    for (int u = 0; u < 8; ++u) T[fidx(32 + r32, c32 + u)] = y[u];
-    __syncthreads();
-}
-
+// ---------------------------------------------------------------- kernel
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                           const float* __restrict__ g_log, const float* __restrict__ beta,
                           float* __restrict__ state, float scale, int Hk, int Hv, int S, int zero_init,
                           int32_t* __restrict__ status) {
-    extern __shared__ uint8_t smem_raw[];
-    Shared sh;
-    sh.base = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    sh.sbase = smem_u32(sh.base);
-    sh.G = reinterpret_cast<float*>(sh.base + OFF_SMALL);
-    sh.gam = sh.G + 64;
-    sh.bet = sh.G + 128;
-    sh.ec = sh.G + 192;
-    sh.bar_tma = reinterpret_cast<uint64_t*>(sh.base + OFF_BAR);
-    sh.bar_mma = sh.bar_tma + 2;
-    sh.tmem_slot = reinterpret_cast<uint32_t*>(sh.bar_mma + 1);
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // Round up to 1024 bytes by indexing the shared array itself, so that every
+    // derived pointer stays a shared-memory pointer (shared loads and stores).
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(sm);
+    Bars* bars = reinterpret_cast<Bars*>(sm + OFF_BAR);
+    float* sG = reinterpret_cast<float*>(sm + OFF_SMALL);
+    float* sGam = sG + 64;
+    float* sBet = sG + 128;
+    float* sEcs = sG + 192;  // [2][64], per stage
+    float* sGC = sG + 320;   // [2], per stage
+    volatile int* abort_flag = &bars->abort;
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -255,329 +278,430 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int bhk = b * Hk + h / (Hv / Hk);
     const int n_chunks = (S + kC - 1) / kC;
 
-    float* As = reinterpret_cast<float*>(sh.base + OFF_OUT);  // fp32 A during the solve
-    float* Ts = reinterpret_cast<float*>(sh.base + OFF_DT);   // fp32 T during the solve
-
     if (tid == 0) {
-        mbar_init(&sh.bar_tma[0], 1);
-        mbar_init(&sh.bar_tma[1], 1);
-        mbar_init(sh.bar_mma, 1);
+        for (int s = 0; s < 2; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->ready[s], kPrep);
+        }
+        mbar_init(&bars->prep_mma, 1);
+        mbar_init(&bars->c1, 1);
+        mbar_init(&bars->c2, 1);
+        mbar_init(&bars->c3, 1);
+        bars->abort = 0;
         fence_mbar_init();
-        tma_prefetch_desc(&tm_q);
-        tma_prefetch_desc(&tm_k);
-        tma_prefetch_desc(&tm_v);
-        tma_prefetch_desc(&tm_o);
     }
     if (warp == 0) {
-        tmem_alloc(sh.tmem_slot, kTmemCols);
+        tmem_alloc(&bars->tmem_base, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *sh.tmem_slot;
-    const uint32_t trow = tmem + ((uint32_t)(warp * 32) << 16);  // this warp's lane quarter
+    const uint32_t tmem = bars->tmem_base;
+    // warp w reads TMEM lanes 32 (w % 4) .. 32 (w % 4) + 31
+    const uint32_t trow = tmem + ((uint32_t)((warp & 3) * 32) << 16);
 
-    // Loads issued so far (chunks [0, issued)); chunks whose loads were consumed: [0, consumed).
-    int issued = 0, consumed = 0;
-    uint32_t mma_phase = 0;
-    bool mma_pending = false;
-    bool failed = false;
-
-    if (tid == 0) {
-        for (; issued < 2 && issued < n_chunks; ++issued)
-            issue_chunk_loads(sh, issued, &tm_q, &tm_k, &tm_v, issued * kC, bhk, bh);
-    }
-
-    // ---- initial state -> TMEM (S^T: lane dv, column dk) and its bf16 copy
-    {
-        const float* Sg = state + (size_t)bh * kD * kD;
-#pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-            float r[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) r[j] = zero_init ? 0.f : Sg[(size_t)(c0 + j) * kD + tid];
-            tmem_st32(trow + COL_S + c0, r);
-            st_row_bf16x32(sh.base + OFF_SB + (c0 >> 6) * 16384, tid, (c0 & 63) * 2, r);
+    if (warp < kPrep / 32) {
+        // ------------------------------------------------------------ prep
+        const int pt = tid;
+        const int L = (warp & 3) * 32 + lane;  // TMEM lane of this thread
+        const int hh = warp >> 2;              // column half (32 columns) of the 64-wide products
+        const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
+        float* M = reinterpret_cast<float*>(sm + OFF_AT);
+        float* X1 = reinterpret_cast<float*>(sm + OFF_SCR + SCR_X1);
+        float* X2 = reinterpret_cast<float*>(sm + OFF_SCR + SCR_X2);
+        uint8_t* t12 = sm + OFF_T12;
+        uint32_t prep_phase = 0;
+        bool mma_pending = false;
+        float g_next = 0.f, b_next = 0.f;  // decay inputs of the coming chunk (threads 0..63)
+        if (pt < 64 && pt < S) {
+            g_next = g_log[(size_t)bh * S + pt];
+            b_next = beta[(size_t)bh * S + pt];
         }
-        tmem_wait_st();
-    }
-    fence_proxy_async_smem();
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-#pragma unroll 1
-    for (int c = 0; c < n_chunks; ++c) {
-        const int stage = c & 1;
-        const uint32_t st_s = sh.sbase + stage * STAGE_BYTES;
-        const int t0 = c * kC;
-
-        // (0) decay scan over the chunk (warps 0, 1: token r = tid)
-        if (tid < 64) {
-            const size_t gi = (size_t)bh * S + t0;
-            const int ta = lane, tb = 32 + lane;
-            float ga = (t0 + ta < S) ? g_log[gi + ta] : 0.f;
-            float gb = (t0 + tb < S) ? g_log[gi + tb] : 0.f;
+        for (int c = 0; c < n_chunks; ++c) {
+            const int s = c & 1;
+            const uint32_t st_s = sbase + s * STAGE_BYTES;
+            uint8_t* st = sm + s * STAGE_BYTES;
+            // ---- chunk inputs; Gram product [K; Q] K^T (runs while the decays are scanned)
+            bool fail = !mbar_wait_or_abort(&bars->full[s], (c >> 1) & 1, abort_flag);
+            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
+            if (pt == 0) {
+                tc_fence_after();
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float ua = __shfl_up_sync(0xffffffffu, ga, o);
-                const float ub = __shfl_up_sync(0xffffffffu, gb, o);
-                if (lane >= o) {
-                    ga += ua;
-                    gb += ub;
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + COL_G, make_sdesc(st_s + ST_K0 + off, 16, 1024),
+                             make_sdesc(st_s + ST_K0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
+                }
+                mma_commit(&bars->prep_mma);
+            }
+            // ---- decays: G = inclusive cumulative sum inside the chunk (threads 0..63)
+            const float g_cur = g_next, b_cur = b_next;
+            if (pt < 64) {
+                const int tn = (c + 1) * kC + pt;
+                g_next = (tn < S) ? g_log[(size_t)bh * S + tn] : 0.f;
+                b_next = (tn < S) ? beta[(size_t)bh * S + tn] : 0.f;
+                float x = g_cur;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const float u = __shfl_up_sync(0xffffffffu, x, o);
+                    if (lane >= o) x += u;
+                }
+                sGam[pt] = x;  // warp partials
+                named_bar_sync(BAR_SCAN, 64);
+                const float G = x + (pt >= 32 ? sGam[31] : 0.f);
+                const float GC = sGam[63] + sGam[31];
+                named_bar_sync(BAR_SCAN, 64);
+                sG[pt] = G * kLog2e;
+                sGam[pt] = exp2_approx(G * kLog2e);
+                sBet[pt] = b_cur;
+                sEcs[64 * s + pt] = exp2_approx((GC - G) * kLog2e);
+                if (pt == 0) sGC[s] = exp2_approx(GC * kLog2e);
+            }
+            mma_pending = true;
+            fail = !mbar_wait_or_abort(&bars->prep_mma, prep_phase, abort_flag);
+            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
+            prep_phase ^= 1;
+            mma_pending = false;
+            tc_fence_after();
+
+            // ---- A (fp32, lanes 0..63) and P (bf16, lanes 64..127); 32 columns per thread
+            {
+                const bool is_a = L < 64;
+                const int r = is_a ? L : L - 64;
+                const int j0 = hh * 32;
+                float x[32];
+                tmem_ld32(trow + COL_G + j0, x);
+                const float Gr = sG[r];
+                const float br = is_a ? sBet[r] : 1.f;
+                const int lim = is_a ? r : r + 1;  // A: j < r, P: j <= r
+                tmem_wait_ld();
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const float4 gj = *reinterpret_cast<const float4*>(sG + j0 + 4 * q);
+                    const float gv[4] = {gj.x, gj.y, gj.z, gj.w};
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const int j = j0 + 4 * q + u;
+                        // exp(G_r - G_j); masked exponents are clamped to 0 so nothing
+                        // overflows before the select
+                        const float e = exp2_approx(fminf(Gr - gv[u], 0.f));
+                        x[4 * q + u] = (j < lim) ? br * e * x[4 * q + u] : 0.f;
+                    }
+                }
+                if (is_a) {
+                    float4* row = reinterpret_cast<float4*>(M + r * AT_STRIDE + j0);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) row[q] = make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
+                } else {
+                    st_row_bf16x32(st + ST_P, r, j0 * 2, x);
                 }
             }
-            const float tot_a = __shfl_sync(0xffffffffu, ga, 31);
-            gb += tot_a;
-            const float gC = __shfl_sync(0xffffffffu, gb, 31);
-            const float gr = warp == 0 ? ga : gb;
-            const int r = tid;
-            sh.G[r] = gr;
-            sh.gam[r] = expf(gr);
-            sh.bet[r] = (t0 + r < S) ? beta[gi + r] : 0.f;
-            sh.ec[r] = expf(gC - gr);
-        }
+            named_bar_sync(BAR_PREP, kPrep);
 
-        // (1) chunk inputs landed -> [K;Q] K^T and S0^T Q^T
-        failed = !mbar_wait(&sh.bar_tma[stage], (c >> 1) & 1);
-        if (__syncthreads_or(failed)) goto abort;
-        consumed = c + 1;
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(tmem + COL_KQ, make_sdesc(st_s + ST_K0 + off, 16, 1024),
-                         make_sdesc(st_s + ST_K0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                mma_bf16(tmem + COL_QS, make_sdesc(sh.sbase + OFF_SB + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                         make_sdesc(st_s + ST_Q0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
-            }
-            mma_commit(sh.bar_mma);
-            tma_store_wait_read0();  // the previous out tile has left the staging area (A reuses it)
-        }
-        mma_pending = true;
-        failed = !mbar_wait(sh.bar_mma, mma_phase);
-        if (__syncthreads_or(failed)) goto abort;
-        mma_phase ^= 1;
-        mma_pending = false;
-        tc_fence_after();
-
-        // (2) A (fp32, lanes 0..63) and P (bf16, lanes 64..127) from the Gram rows
-        {
-            float x0[32], x1[32];
-            tmem_ld32(trow + COL_KQ, x0);
-            tmem_ld32(trow + COL_KQ + 32, x1);
-            tmem_wait_ld();
-            if (tid < 64) {
-                const int r = tid;
-                const float Gr = sh.G[r], br = sh.bet[r];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) As[fidx(r, j)] = (j < r) ? br * expf(Gr - sh.G[j]) * x0[j] : 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j)
-                    As[fidx(r, 32 + j)] = (32 + j < r) ? br * expf(Gr - sh.G[32 + j]) * x1[j] : 0.f;
+            // ---- warps 0..3: diagonal blocks of T;  warps 4..7: Q' = diag(gamma) Q in place
+            if (warp < 4) {
+                solve_diag_block(M, warp, lane);
             } else {
-                const int r = tid - 64;
-                const float Gr = sh.G[r];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x0[j] = (j <= r) ? expf(Gr - sh.G[j]) * x0[j] : 0.f;
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x1[j] = (32 + j <= r) ? expf(Gr - sh.G[32 + j]) * x1[j] : 0.f;
-                st_row_bf16x32(sh.base + OFF_P, r, 0, x0);
-                st_row_bf16x32(sh.base + OFF_P, r, 64, x1);
+                const int qt = pt - 128;  // 0..127: row qt / 2 of the Q box qt % 2
+                scale_row_chunks<8>(st + ((qt & 1) ? ST_Q1 : ST_Q0), qt >> 1, 0, sGam[qt >> 1]);
             }
-        }
-        __syncthreads();
-
-        // (3) T = (I + A)^-1 (fp32), then T diag(beta) and T diag(beta gamma) as bf16
-        solve_unit_lower_64(As, Ts, tid);
-        {
-            const int r = tid >> 1, j0 = (tid & 1) * 32;
-            float t1[32], t2[32];
+            named_bar_sync(BAR_PREP, kPrep);
+            if (warp < 4) {
+                // ---- level 1 (warps 0..3): T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22
+                const int blk = warp >> 1, nt = warp & 1;
+                const int rb = 32 * blk + 16, cb = 32 * blk;
+                float* xs = X1 + warp * 128;  // 16 x 8, stride 8
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float t = Ts[fidx(r, j0 + j)];
-                const float bj = sh.bet[j0 + j];
-                t1[j] = t * bj;
-                t2[j] = t * bj * sh.gam[j0 + j];
+                for (int ks = 0; ks < 2; ++ks) {
+                    if (ks < nt) continue;  // T_bb is lower triangular
+                    uint32_t a[4], bf[2];
+                    load_afrag(M, AT_STRIDE, rb, cb + 8 * ks, g, t, a);
+                    load_bfrag(M, AT_STRIDE, cb + 8 * ks, cb + 8 * nt, g, t, bf);
+                    mma_tf32_16x8x8(d, a, bf);
+                }
+                store_cfrag(xs, 8, 0, 0, g, t, d, 1.f);
+                named_bar_sync(BAR_L1, 128);  // every X tile is out of A's block before T overwrites it
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+                for (int ks = 0; ks < 2; ++ks) {
+                    uint32_t a[4], bf[2];
+                    load_afrag(M, AT_STRIDE, rb, rb + 8 * ks, g, t, a);
+                    load_bfrag(xs, 8, 8 * ks, 0, g, t, bf);
+                    mma_tf32_16x8x8(y, a, bf);
+                }
+                store_cfrag(M, AT_STRIDE, rb, cb + 8 * nt, g, t, y, -1.f);
+                store_t12_frag(t12, sBet, sGam, rb, cb + 8 * nt, g, t, y, -1.f);
+            } else {
+                // ---- warps 4..7 meanwhile: the diagonal blocks and the zero upper blocks of
+                //      T diag(beta), T diag(beta gamma); row qt / 2, 16-byte chunks 4 (qt % 2) ..
+                const int qt = pt - 128;
+                const int r = qt >> 1, br = r >> 4;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int q = 4 * (qt & 1) + i;  // chunk = columns 8q .. 8q + 7
+                    const int bc = q >> 1;           // 16-column block of the chunk
+                    if (bc < br) continue;           // below the diagonal: written by levels 1, 2
+                    uint4 w1 = make_uint4(0u, 0u, 0u, 0u), w2 = w1;
+                    if (bc == br) {
+                        const float4 t0 = *reinterpret_cast<const float4*>(M + r * AT_STRIDE + 8 * q);
+                        const float4 t1 = *reinterpret_cast<const float4*>(M + r * AT_STRIDE + 8 * q + 4);
+                        const float tv[8] = {t0.x, t0.y, t0.z, t0.w, t1.x, t1.y, t1.z, t1.w};
+                        float a1[8], a2[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) {
+                            a1[u] = tv[u] * sBet[8 * q + u];
+                            a2[u] = a1[u] * sGam[8 * q + u];
+                        }
+                        w1 = make_uint4(pack_bf16x2(a1[0], a1[1]), pack_bf16x2(a1[2], a1[3]), pack_bf16x2(a1[4], a1[5]),
+                                        pack_bf16x2(a1[6], a1[7]));
+                        w2 = make_uint4(pack_bf16x2(a2[0], a2[1]), pack_bf16x2(a2[2], a2[3]), pack_bf16x2(a2[4], a2[5]),
+                                        pack_bf16x2(a2[6], a2[7]));
+                    }
+                    const uint32_t off = sw128_offset(r, 16 * q);
+                    *reinterpret_cast<uint4*>(t12 + off) = w1;
+                    *reinterpret_cast<uint4*>(t12 + 8192 + off) = w2;
+                }
             }
-            st_row_bf16x32(sh.base + OFF_T1, r, j0 * 2, t1);
-            st_row_bf16x32(sh.base + OFF_T2, r, j0 * 2, t2);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // (4) U^T = V^T T1^T,  W^T = K^T T2^T
-        if (tid == 0) {
-            tc_fence_after();
+            named_bar_sync(BAR_PREP, kPrep);
+            // ---- level 2 (8 warps, one 16 x 8 tile each):
+            //      X = A[32:64, 0:32] T[0:32, 0:32];  T[32:64, 0:32] = -T[32:64, 32:64] X
+            {
+                const int mt = warp >> 2, nt = warp & 3;
+                float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + COL_U, make_sdesc(st_s + ST_V0 + kk * 2048, 8192, 1024),
-                         make_sdesc(sh.sbase + OFF_T1 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+                for (int ks = 0; ks < 4; ++ks) {
+                    if (ks < nt) continue;  // T[0:32, 0:32] is lower triangular
+                    uint32_t a[4], bf[2];
+                    load_afrag(M, AT_STRIDE, 32 + 16 * mt, 8 * ks, g, t, a);
+                    load_bfrag(M, AT_STRIDE, 8 * ks, 8 * nt, g, t, bf);
+                    mma_tf32_16x8x8(d, a, bf);
+                }
+                store_cfrag(X2, X2_STRIDE, 16 * mt, 8 * nt, g, t, d, 1.f);
+                named_bar_sync(BAR_PREP, kPrep);
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + COL_W, make_sdesc(st_s + ST_K0 + kk * 2048, 16384, 1024),
-                         make_sdesc(sh.sbase + OFF_T2 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
-            mma_commit(sh.bar_mma);
-        }
-        mma_pending = true;
-        failed = !mbar_wait(sh.bar_mma, mma_phase);
-        if (__syncthreads_or(failed)) goto abort;
-        mma_phase ^= 1;
-        mma_pending = false;
-        tc_fence_after();
-
-        // (5) -W as the MN-major B operand: row dk = tid, 64 token values
-        {
-            float x0[32], x1[32];
-            tmem_ld32(trow + COL_W, x0);
-            tmem_ld32(trow + COL_W + 32, x1);
-            tmem_wait_ld();
-            st_row_bf16x32(sh.base + OFF_WD, tid, 0, x0, -1.f);
-            st_row_bf16x32(sh.base + OFF_WD, tid, 64, x1, -1.f);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // (6) Delta^T = U^T + S0^T (-W)^T
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                mma_bf16(tmem + COL_U, make_sdesc(sh.sbase + OFF_SB + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                         make_sdesc(sh.sbase + OFF_WD + kk * 2048, 8192, 1024), IDESC_N64_KM, 1);
-            mma_commit(sh.bar_mma);
-        }
-        mma_pending = true;
-        failed = !mbar_wait(sh.bar_mma, mma_phase);
-        if (__syncthreads_or(failed)) goto abort;
-        mma_phase ^= 1;
-        mma_pending = false;
-        tc_fence_after();
-
-        // (7) Delta^T and Delta~^T = Delta^T diag(exp(G_C - G)) as K-major A operands (row dv = tid)
-        {
-            float x0[32], x1[32];
-            tmem_ld32(trow + COL_U, x0);
-            tmem_ld32(trow + COL_U + 32, x1);
-            tmem_wait_ld();
-            st_row_bf16x32(sh.base + OFF_WD, tid, 0, x0);
-            st_row_bf16x32(sh.base + OFF_WD, tid, 64, x1);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                x0[j] *= sh.ec[j];
-                x1[j] *= sh.ec[32 + j];
+                for (int ks = 0; ks < 4; ++ks) {
+                    if (ks >= 2 * mt + 2) continue;  // T[32:64, 32:64] is lower triangular
+                    uint32_t a[4], bf[2];
+                    load_afrag(M, AT_STRIDE, 32 + 16 * mt, 32 + 8 * ks, g, t, a);
+                    load_bfrag(X2, X2_STRIDE, 8 * ks, 8 * nt, g, t, bf);
+                    mma_tf32_16x8x8(y, a, bf);
+                }
+                store_t12_frag(t12, sBet, sGam, 32 + 16 * mt, 8 * nt, g, t, y, -1.f);
             }
-            st_row_bf16x32(sh.base + OFF_DT, tid, 0, x0);
-            st_row_bf16x32(sh.base + OFF_DT, tid, 64, x1);
-        }
-        fence_proxy_async_smem();
-        tc_fence_before();
-        __syncthreads();
-
-        // (8) R_PD = Delta^T P^T,  R_SN = Delta~^T K
-        if (tid == 0) {
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar_sync(BAR_PREP, kPrep);
+            // ---- U^T = V^T (T diag beta)^T,  W^T = K^T (T diag beta gamma)^T
+            if (pt == 0) {
+                tc_fence_after();
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + COL_U + 64 * s, make_sdesc(st_s + ST_V + kk * 2048, 8192, 1024),
+                             make_sdesc(sbase + OFF_T12 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + COL_W, make_sdesc(st_s + ST_K0 + kk * 2048, 16384, 1024),
+                             make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+                mma_commit(&bars->prep_mma);
+            }
+            mma_pending = true;
+            fail = !mbar_wait_or_abort(&bars->prep_mma, prep_phase, abort_flag);
+            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
+            prep_phase ^= 1;
+            mma_pending = false;
             tc_fence_after();
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + COL_KQ, make_sdesc(sh.sbase + OFF_WD + kk * 32, 16, 1024),
-                         make_sdesc(sh.sbase + OFF_P + kk * 32, 16, 1024), IDESC_N64_KK, kk > 0);
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk)
-                mma_bf16(tmem + COL_SN, make_sdesc(sh.sbase + OFF_DT + kk * 32, 16, 1024),
-                         make_sdesc(st_s + ST_K0 + kk * 2048, 16384, 1024), IDESC_N128_KM, kk > 0);
-            mma_commit(sh.bar_mma);
+            // ---- -W over V (the U product has read V): row dk = L, 32 token columns
+            {
+                float x[32];
+                tmem_ld32(trow + COL_W + hh * 32, x);
+                tmem_wait_ld();
+                st_row_bf16x32(st + ST_V, L, hh * 64, x, -1.f);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bars->ready[s]);
         }
-        mma_pending = true;
-        failed = !mbar_wait(sh.bar_mma, mma_phase);
-        if (__syncthreads_or(failed)) goto abort;
-        mma_phase ^= 1;
-        mma_pending = false;
-        tc_fence_after();
-
-        // (9) state S^T <- gamma_C S^T + R_SN (fp32 in TMEM) and its bf16 copy
+        if (mma_pending) (void)mbar_wait(&bars->prep_mma, prep_phase);
+    } else {
+        // ------------------------------------------------------------ chain
+        const int ct = tid - kPrep;  // dv row = TMEM lane
         {
-            const float gC = sh.gam[kC - 1];
+            const float* Sg = state + (size_t)bh * kD * kD;
 #pragma unroll 1
             for (int c0 = 0; c0 < kD; c0 += 32) {
-                float s[32], dn[32];
-                tmem_ld32(trow + COL_S + c0, s);
-                tmem_ld32(trow + COL_SN + c0, dn);
-                tmem_wait_ld();
+                float x[32];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) s[j] = fmaf(gC, s[j], dn[j]);
-                tmem_st32(trow + COL_S + c0, s);
-                st_row_bf16x32(sh.base + OFF_SB + (c0 >> 6) * 16384, tid, (c0 & 63) * 2, s);
+                for (int j = 0; j < 32; ++j) x[j] = zero_init ? 0.f : Sg[(size_t)(c0 + j) * kD + ct];
+                tmem_st32(trow + COL_S + c0, x);
+                st_row_bf16x32(sm + OFF_SB + (c0 >> 6) * 16384, ct, (c0 & 63) * 2, x);
             }
+            tmem_wait_st();
         }
-        // (10) output O^T[dv][r] = scale (gamma_r R_QS + R_PD) -> bf16 tile [r][dv]
-        {
-            uint8_t* ob = sh.base + OFF_OUT + (tid >> 6) * 8192;
-            const uint32_t cb = (uint32_t)(tid & 63) * 2;
-#pragma unroll 1
-            for (int r0 = 0; r0 < kC; r0 += 32) {
-                float qs[32], pd[32];
-                tmem_ld32(trow + COL_QS + r0, qs);
-                tmem_ld32(trow + COL_KQ + r0, pd);
-                tmem_wait_ld();
-#pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                    const float o = scale * fmaf(sh.gam[r0 + j], qs[j], pd[j]);
-                    *reinterpret_cast<__nv_bfloat16*>(ob + sw128_offset(r0 + j, cb)) = __float2bfloat16_rn(o);
-                }
+        int last_load[2] = {-1, -1};  // last chunk loaded into each stage (thread ct == 32 loads)
+        if (ct == 32) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_o);
+            for (int c = 0; c < 2 && c < n_chunks; ++c) {
+                load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, c, bhk, bh);
+                last_load[c] = c;
             }
+            if (n_chunks > 2) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, 2, bhk, bh);
         }
-        tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
-        __syncthreads();
-        if (tid == 0) {
-            tma_store_3d(&tm_o, sh.base + OFF_OUT, 0, t0, bh);
-            tma_store_3d(&tm_o, sh.base + OFF_OUT + 8192, 64, t0, bh);
-            tma_store_commit();
-            if (issued < n_chunks) {  // this stage's tiles are no longer read by any MMA
-                issue_chunk_loads(sh, stage, &tm_q, &tm_k, &tm_v, issued * kC, bhk, bh);
-                ++issued;
+        named_bar_sync(BAR_CHAIN, kChain);
+        int issued1 = -1, issued23 = -1;  // last chunk whose chain MMAs were committed
+        bool ok = true;
+        for (int c = 0; c < n_chunks && ok; ++c) {
+            const int s = c & 1;
+            const uint32_t st_s = sbase + s * STAGE_BYTES;
+            bool fail = !mbar_wait_or_abort(&bars->ready[s], (c >> 1) & 1, abort_flag);
+            if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
+            const float gC = sGC[s];
+            tc_fence_after();
+            if (ct == 0) {
+                // Delta^T = U^T + S0^T (-W)^T
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk)
+                    mma_bf16(tmem + COL_U + 64 * s,
+                             make_sdesc(sbase + OFF_SB + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                             make_sdesc(st_s + ST_V + kk * 2048, 8192, 1024), IDESC_N64_KM, 1);
+                mma_commit(&bars->c1);
+                // O^T = S0^T Q'^T (first part of the output)
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
+                    mma_bf16(tmem + COL_O + 64 * s, make_sdesc(sbase + OFF_SB + off, 16, 1024),
+                             make_sdesc(st_s + ST_Q0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
+                }
+            }
+            issued1 = c;
+            // K~ = diag(exp(G_C - G)) K in place while the products run (prep's W product has
+            // read K; the state increment below reads K~): row ct / 2 of box ct % 2
+            scale_row_chunks<8>(sm + s * STAGE_BYTES + ((ct & 1) ? ST_K1 : ST_K0), ct >> 1, 0, sEcs[64 * s + (ct >> 1)]);
+            // S^T <- gamma_C S^T in TMEM while the products run; the increment accumulates onto it
+#pragma unroll 1
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                float x[32];
+                tmem_ld32(trow + COL_S + c0, x);
+                tmem_wait_ld();
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] *= gC;
+                tmem_st32(trow + COL_S + c0, x);
+            }
+            tmem_wait_st();
+            fail = !mbar_wait_or_abort(&bars->c1, c & 1, abort_flag);
+            if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
+            tc_fence_after();
+            {
+                float x[32];
+                tmem_ld32(trow + COL_U + 64 * s, x);
+                tmem_wait_ld();
+                st_row_bf16x32(sm + OFF_DT, ct, 0, x);
+                tmem_ld32(trow + COL_U + 64 * s + 32, x);
+                tmem_wait_ld();
+                st_row_bf16x32(sm + OFF_DT, ct, 64, x);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (ct == 0) tma_store_wait_read0();  // the out tile of chunk c-2 has been read
+            named_bar_sync(BAR_CHAIN, kChain);
+            if (ct == 0) {
+                tc_fence_after();
+                // S^T += Delta^T K~
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + COL_S, make_sdesc(sbase + OFF_DT + kk * 32, 16, 1024),
+                             make_sdesc(st_s + ST_K0 + kk * 2048, 16384, 1024), IDESC_N128_KM, 1);
+                mma_commit(&bars->c2);
+                // O^T += Delta^T P^T
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_bf16(tmem + COL_O + 64 * s, make_sdesc(sbase + OFF_DT + kk * 32, 16, 1024),
+                             make_sdesc(st_s + ST_P + kk * 32, 16, 1024), IDESC_N64_KK, 1);
+                mma_commit(&bars->c3);
+            }
+            issued23 = c;
+            // output of the previous chunk (its accumulator completed last iteration)
+            if (c >= 1) write_out_tile(sm + OFF_OUT, trow + COL_O + 64 * ((c - 1) & 1), ct, scale);
+            fail = !mbar_wait_or_abort(&bars->c2, c & 1, abort_flag);
+            if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
+            tc_fence_after();
+            if (ct == 32) {
+                // once the output product has completed, every read of this stage is done:
+                // reload it with chunk c + 2 and prefetch chunk c + 3 into L2
+                // (a failed wait has set the abort flag, which every role checks)
+                if (mbar_wait_or_abort(&bars->c3, c & 1, abort_flag) && c + 2 < n_chunks) {
+                    load_chunk(sm + s * STAGE_BYTES, &bars->full[s], &tm_q, &tm_k, &tm_v, c + 2, bhk, bh);
+                    last_load[s] = c + 2;
+                    if (c + 3 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, c + 3, bhk, bh);
+                }
+            }
+            // bf16 copy of the new state for the next chunk's products
+#pragma unroll 1
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                float x[32];
+                tmem_ld32(trow + COL_S + c0, x);
+                tmem_wait_ld();
+                st_row_bf16x32(sm + OFF_SB + (c0 >> 6) * 16384, ct, (c0 & 63) * 2, x);
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            named_bar_sync(BAR_CHAIN, kChain);
+            if (ct == 0 && c >= 1) {  // out tile of chunk c - 1
+                tma_store_3d(&tm_o, sm + OFF_OUT, 0, (c - 1) * kC, bh);
+                tma_store_commit();
             }
         }
-    }
-
-    // ---- final state S[dk][dv] = S^T[dv][dk] (coalesced across a warp)
-    {
-        tc_fence_after();
-        float* Sg = state + (size_t)bh * kD * kD;
+        ok = !named_bar_any(BAR_CHAIN, kChain, !ok || *abort_flag != 0);
+        if (ok && n_chunks > 0) {
+            // output of the last chunk (its product was waited for above), then the final state
+            const int c = n_chunks - 1;
+            if (ct == 0) {
+                tma_store_wait_read0();
+                (void)mbar_wait(&bars->c3, c & 1);  // completed already (waited for inside the loop)
+            }
+            named_bar_sync(BAR_CHAIN, kChain);
+            write_out_tile(sm + OFF_OUT, trow + COL_O + 64 * (c & 1), ct, scale);
+            fence_proxy_async_smem();
+            named_bar_sync(BAR_CHAIN, kChain);
+            if (ct == 0) {
+                tma_store_3d(&tm_o, sm + OFF_OUT, 0, c * kC, bh);
+                tma_store_commit();
+            }
+            float* Sg = state + (size_t)bh * kD * kD;
 #pragma unroll 1
-        for (int c0 = 0; c0 < kD; c0 += 32) {
-            float s[32];
-            tmem_ld32(trow + COL_S + c0, s);
-            tmem_wait_ld();
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                float x[32];
+                tmem_ld32(trow + COL_S + c0, x);
+                tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 32; ++j) Sg[(size_t)(c0 + j) * kD + tid] = s[j];
+                for (int j = 0; j < 32; ++j) Sg[(size_t)(c0 + j) * kD + ct] = x[j];
+            }
         }
+        if (!ok) {  // drain what we issued (waiting on a completed phase returns at once)
+            if (ct == 0) {
+                if (issued1 >= 0) (void)mbar_wait(&bars->c1, issued1 & 1);
+                if (issued23 >= 0) {
+                    (void)mbar_wait(&bars->c2, issued23 & 1);
+                    (void)mbar_wait(&bars->c3, issued23 & 1);
+                }
+            }
+            if (ct == 32)
+                for (int st = 0; st < 2; ++st)
+                    if (last_load[st] >= 0) (void)mbar_wait(&bars->full[st], (last_load[st] >> 1) & 1);
+        }
+        if (ct == 0) tma_store_wait_all0();
     }
-    if (tid == 0) tma_store_wait_all0();
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
-    return;
 
-abort:
-    // A wait gave up: record it, drain what is still in flight (bounded), free TMEM.
-    if (tid == 0) {
-        atomicExch(status, (int32_t)GDN_ERR_TIMEOUT);
-        for (int cc = consumed; cc < issued; ++cc) (void)mbar_wait(&sh.bar_tma[cc & 1], (cc >> 1) & 1);
-        if (mma_pending) (void)mbar_wait(sh.bar_mma, mma_phase);
-        tma_store_wait_all0();
-    }
     tc_fence_before();
     __syncthreads();
+    if (tid == 0 && bars->abort) atomicExch(status, (int32_t)GDN_ERR_TIMEOUT);
     if (warp == 0) tmem_dealloc(tmem, kTmemCols);
 }
 
@@ -600,17 +724,17 @@ EncodeTiledFn get_encode_fn() {
     return fn;
 }
 
-// [heads, S, 128] bf16 viewed as a 3-D tensor (128 innermost), box 64 x 64 x 1.
-bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S) {
+// [heads, S, 128] bf16 viewed as a 3-D tensor (128 innermost).
+bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_t box_inner, bool swizzle) {
     EncodeTiledFn enc = get_encode_fn();
     if (!enc) return false;
     cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)S, (cuuint64_t)heads};
     cuuint64_t strides[2] = {(cuuint64_t)kD * 2, (cuuint64_t)S * kD * 2};
-    cuuint32_t box[3] = {64, 64, 1};
+    cuuint32_t box[3] = {box_inner, (cuuint32_t)kC, 1};
     cuuint32_t estr[3] = {1, 1, 1};
     return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
-               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+               CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -619,8 +743,9 @@ bool prefill_tc_supported(const Problem& p) { return p.bf16 && p.Dk == kD && p.D
 
 gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_t stream) {
     CUtensorMap tq, tk, tv, to;
-    if (!encode_bf16_3d(&tq, p.q, p.B * p.Hk, p.S) || !encode_bf16_3d(&tk, p.k, p.B * p.Hk, p.S) ||
-        !encode_bf16_3d(&tv, p.v, p.B * p.Hv, p.S) || !encode_bf16_3d(&to, p.out, p.B * p.Hv, p.S))
+    if (!encode_bf16_3d(&tq, p.q, p.B * p.Hk, p.S, 64, true) || !encode_bf16_3d(&tk, p.k, p.B * p.Hk, p.S, 64, true) ||
+        !encode_bf16_3d(&tv, p.v, p.B * p.Hv, p.S, 64, true) ||
+        !encode_bf16_3d(&to, p.out, p.B * p.Hv, p.S, 128, false))
         return GDN_ERR_CUDA;
     if (cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              (int)SMEM_ALLOC) != cudaSuccess)
