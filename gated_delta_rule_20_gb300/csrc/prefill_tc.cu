@@ -20,11 +20,12 @@
 // Orientation.  Every tensor-core product is issued with M = 128 by putting a
 // head dimension (Dv or Dk = 128) on the M / TMEM-lane axis and the chunk's 64
 // tokens on N:
-//     R_G    = [K; Q] K^T       (lanes 0..63: K K^T rows, 64..127: Q K^T rows)
-//     R_U[s] = V^T (T diag beta)^T               -> U^T
+//     R_G    = [Q; K] K^T       (lanes 0..63: Q K^T rows, 64..127: K K^T rows)
+//     R_D[s] = [V^T (T diag beta)^T | 0]          -> [U^T | 0]
 //     R_W    = K^T (T diag beta gamma)^T         -> W^T
-//     R_U[s] += S0^T (-W)^T                      -> Delta^T   (chain)
-//     R_O[s] = S0^T Q'^T + Delta^T P^T           -> O^T / scale (chain)
+//     R_D[s] += S0^T [-W; Q']^T  (one N = 128 product, chain)
+//                                                -> [Delta^T | S0^T Q'^T]
+//     R_D[s] right half += Delta^T P^T           -> O^T / scale (chain)
 //     R_S   += Delta^T K~                        -> state increment, S^T layout
 //
 // Roles (one CTA per (batch, value head), 384 threads):
@@ -71,20 +72,24 @@ constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns (fp32, 128 lanes each)
 constexpr uint32_t COL_G = 0;    // 64: Gram
-constexpr uint32_t COL_U = 64;   // 2 x 64: U^T then Delta^T, per stage
-constexpr uint32_t COL_W = 192;  // 64: W^T
-constexpr uint32_t COL_O = 256;  // 2 x 64: output accumulators, per stage
+constexpr uint32_t COL_W = 64;   // 64: W^T
+constexpr uint32_t COL_D = 128;  // 2 x 128, per stage: [U^T -> Delta^T | output accumulator]
 constexpr uint32_t COL_S = 384;  // 128: the fp32 state S^T (lane dv, column dk)
 
 // Shared memory (bytes from a 1024-aligned base).  bf16 tiles: rows of 128 B
 // with the 128-byte swizzle.
+// Stage: per 64-wide half h of the head dims, three [64 tokens][64] boxes
+// [V (dv half h), later -W (dk half h, K-major) | Q | K], then P.  [-W; Q'] and
+// [Q; K] are each one contiguous 128-row K-major operand.
 constexpr uint32_t STAGE_BYTES = 57344;
-constexpr uint32_t ST_K0 = 0;      // K (-> K~), dk 0..63     [64 tokens][64]
-constexpr uint32_t ST_Q0 = 8192;   // Q (-> Q'), dk 0..63
-constexpr uint32_t ST_K1 = 16384;  // K (-> K~), dk 64..127
-constexpr uint32_t ST_Q1 = 24576;  // Q (-> Q'), dk 64..127
-constexpr uint32_t ST_V = 32768;   // V as two [64][64] boxes; then -W as [128 dk][64 r]
-constexpr uint32_t ST_P = 49152;   // P [64 r][64 j]
+constexpr uint32_t ST_HALF = 24576;  // distance between the two halves
+constexpr uint32_t ST_VW0 = 0;       // V dv 0..63, then -W [64 r][dk 0..63]
+constexpr uint32_t ST_Q0 = 8192;     // Q (-> Q'), dk 0..63
+constexpr uint32_t ST_K0 = 16384;    // K (-> K~), dk 0..63
+constexpr uint32_t ST_VW1 = ST_VW0 + ST_HALF;
+constexpr uint32_t ST_Q1 = ST_Q0 + ST_HALF;
+constexpr uint32_t ST_K1 = ST_K0 + ST_HALF;
+constexpr uint32_t ST_P = 49152;     // P [64 r][64 j]
 constexpr uint32_t LOAD_BYTES = 49152;
 constexpr uint32_t OFF_T12 = 2 * STAGE_BYTES;  // T diag(beta), T diag(beta gamma): [64 r][64 j] bf16 each
 constexpr uint32_t OFF_AT = OFF_T12 + 16384;   // fp32 A, solved in place into T: [64][68]
@@ -95,8 +100,9 @@ constexpr uint32_t OFF_OUT = OFF_DT + 16384;   // out tile [64 r][128 dv] bf16, 
 constexpr uint32_t OFF_SCR = OFF_OUT + 16384;   // solve scratch (fp32 X tiles)
 constexpr uint32_t OFF_SMALL = OFF_SCR + 8192;
 // small area (floats): G2[64] = log2(e) x cumulative log-decay, gam[64], bet[64],
-// ec[2][64] (per stage: read late in the chunk), gC[2]
-constexpr uint32_t OFF_BAR = OFF_SMALL + 1536;
+// then per chunk c in slot c % 3 (written one chunk ahead, read by the chain):
+// ec[3][64] = exp(G_C - G), gC[3] = exp(G_C)
+constexpr uint32_t OFF_BAR = OFF_SMALL + 1792;
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(OFF_SB % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_OUT % 1024 == 0, "tile alignment");
@@ -108,8 +114,8 @@ constexpr int X2_STRIDE = 40;
 
 constexpr uint32_t IDESC_N64_KK = make_idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t IDESC_N64_MK = make_idesc_bf16(128, 64, 1, 0);   // A MN-major
-constexpr uint32_t IDESC_N64_KM = make_idesc_bf16(128, 64, 0, 1);   // B MN-major
-constexpr uint32_t IDESC_N128_KM = make_idesc_bf16(128, 128, 0, 1);
+constexpr uint32_t IDESC_N128_KK = make_idesc_bf16(128, 128, 0, 0);
+constexpr uint32_t IDESC_N128_KM = make_idesc_bf16(128, 128, 0, 1);  // B MN-major
 
 constexpr uint32_t BAR_PREP = 1;   // named barrier: the 8 prep warps
 constexpr uint32_t BAR_CHAIN = 2;  // named barrier: the 4 chain warps
@@ -166,7 +172,9 @@ __device__ __forceinline__ void write_out_tile(uint8_t* tile, uint32_t taddr, in
 struct Bars {
     uint64_t full[2];   // TMA -> prep
     uint64_t ready[2];  // prep -> chain (kPrep arrivals)
-    uint64_t prep_mma;  // prep's MMA commits
+    uint64_t dfree[2];  // chain has read R_D[s] (its output) -> prep may rewrite it (kChain arrivals)
+    uint64_t gram;      // prep: Gram product of a chunk done
+    uint64_t prep_mma;  // prep: U, W products done
     uint64_t c1;        // chain: Delta product done
     uint64_t c2;        // chain: state increment done
     uint64_t c3;        // chain: output accumulator done
@@ -235,8 +243,8 @@ __device__ __forceinline__ void load_chunk(uint8_t* st, uint64_t* bar, const CUt
     tma_load_3d(st + ST_Q0, tq, bar, 0, t0, bhk);
     tma_load_3d(st + ST_K1, tk, bar, 64, t0, bhk);
     tma_load_3d(st + ST_Q1, tq, bar, 64, t0, bhk);
-    tma_load_3d(st + ST_V, tv, bar, 0, t0, bh);
-    tma_load_3d(st + ST_V + 8192, tv, bar, 64, t0, bh);
+    tma_load_3d(st + ST_VW0, tv, bar, 0, t0, bh);
+    tma_load_3d(st + ST_VW1, tv, bar, 64, t0, bh);
 }
 __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
                                                   int c, int bhk, int bh) {
@@ -265,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sG = reinterpret_cast<float*>(sm + OFF_SMALL);
     float* sGam = sG + 64;
     float* sBet = sG + 128;
-    float* sEcs = sG + 192;  // [2][64], per stage
-    float* sGC = sG + 320;   // [2], per stage
+    float* sEcs = sG + 192;  // [3][64], slot c % 3
+    float* sGC = sG + 384;   // [3], slot c % 3
     volatile int* abort_flag = &bars->abort;
 
     const int tid = threadIdx.x;
@@ -282,7 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->ready[s], kPrep);
+            mbar_init(&bars->dfree[s], kChain);
         }
+        mbar_init(&bars->gram, 1);
         mbar_init(&bars->prep_mma, 1);
         mbar_init(&bars->c1, 1);
         mbar_init(&bars->c2, 1);
@@ -313,62 +323,69 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint8_t* t12 = sm + OFF_T12;
         uint32_t prep_phase = 0;
         bool mma_pending = false;
-        float g_next = 0.f, b_next = 0.f;  // decay inputs of the coming chunk (threads 0..63)
-        if (pt < 64 && pt < S) {
-            g_next = g_log[(size_t)bh * S + pt];
-            b_next = beta[(size_t)bh * S + pt];
+        int gram_issued = -1, gram_waited = -1;
+        // Gram product [Q; K] K^T of chunk cc into R_G (issued by thread 64 once the chunk has landed)
+        auto issue_gram = [&](int cc) {
+            const uint32_t st_c = sbase + (cc & 1) * STAGE_BYTES;
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                const uint32_t off = (kk >> 2) * ST_HALF + (kk & 3) * 32;
+                mma_bf16(tmem + COL_G, make_sdesc(st_c + ST_Q0 + off, 16, 1024),
+                         make_sdesc(st_c + ST_K0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
+            }
+            mma_commit(&bars->gram);
+        };
+        // decays of chunk cc (threads 0..63): G = inclusive cumulative sum inside the chunk
+        auto scan_decays = [&](int cc, float gv, float bv) {
+            float x = gv;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const float u = __shfl_up_sync(0xffffffffu, x, o);
+                if (lane >= o) x += u;
+            }
+            sGam[pt] = x;  // warp partials
+            named_bar_sync(BAR_SCAN, 64);
+            const float G = x + (pt >= 32 ? sGam[31] : 0.f);
+            const float GC = sGam[63] + sGam[31];
+            named_bar_sync(BAR_SCAN, 64);
+            sG[pt] = G * kLog2e;
+            sGam[pt] = exp2_approx(G * kLog2e);
+            sBet[pt] = bv;
+            sEcs[64 * (cc % 3) + pt] = exp2_approx((GC - G) * kLog2e);
+            if (pt == 0) sGC[cc % 3] = exp2_approx(GC * kLog2e);
+        };
+        // decay inputs: chunk 0 now, chunk 1 prefetched (threads 0..63)
+        float g_next = 0.f, b_next = 0.f;
+        if (pt < 64) {
+            const float g0 = (pt < S) ? g_log[(size_t)bh * S + pt] : 0.f;
+            const float b0 = (pt < S) ? beta[(size_t)bh * S + pt] : 0.f;
+            g_next = (kC + pt < S) ? g_log[(size_t)bh * S + kC + pt] : 0.f;
+            b_next = (kC + pt < S) ? beta[(size_t)bh * S + kC + pt] : 0.f;
+            scan_decays(0, g0, b0);
+        }
+        if (pt == 64 && n_chunks > 0) {
+            if (mbar_wait_or_abort(&bars->full[0], 0, abort_flag)) {
+                issue_gram(0);
+                gram_issued = 0;
+            }
         }
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c & 1;
             const uint32_t st_s = sbase + s * STAGE_BYTES;
             uint8_t* st = sm + s * STAGE_BYTES;
-            // ---- chunk inputs; Gram product [K; Q] K^T (runs while the decays are scanned)
+            // ---- chunk inputs have landed (the Gram product was issued at the end of the
+            //      previous chunk; every thread still observes the load's completion)
             bool fail = !mbar_wait_or_abort(&bars->full[s], (c >> 1) & 1, abort_flag);
+            if (!fail) fail = !mbar_wait_or_abort(&bars->gram, c & 1, abort_flag);
             if (named_bar_any(BAR_PREP, kPrep, fail)) break;
-            if (pt == 0) {
-                tc_fence_after();
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + COL_G, make_sdesc(st_s + ST_K0 + off, 16, 1024),
-                             make_sdesc(st_s + ST_K0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
-                }
-                mma_commit(&bars->prep_mma);
-            }
-            // ---- decays: G = inclusive cumulative sum inside the chunk (threads 0..63)
-            const float g_cur = g_next, b_cur = b_next;
-            if (pt < 64) {
-                const int tn = (c + 1) * kC + pt;
-                g_next = (tn < S) ? g_log[(size_t)bh * S + tn] : 0.f;
-                b_next = (tn < S) ? beta[(size_t)bh * S + tn] : 0.f;
-                float x = g_cur;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float u = __shfl_up_sync(0xffffffffu, x, o);
-                    if (lane >= o) x += u;
-                }
-                sGam[pt] = x;  // warp partials
-                named_bar_sync(BAR_SCAN, 64);
-                const float G = x + (pt >= 32 ? sGam[31] : 0.f);
-                const float GC = sGam[63] + sGam[31];
-                named_bar_sync(BAR_SCAN, 64);
-                sG[pt] = G * kLog2e;
-                sGam[pt] = exp2_approx(G * kLog2e);
-                sBet[pt] = b_cur;
-                sEcs[64 * s + pt] = exp2_approx((GC - G) * kLog2e);
-                if (pt == 0) sGC[s] = exp2_approx(GC * kLog2e);
-            }
-            mma_pending = true;
-            fail = !mbar_wait_or_abort(&bars->prep_mma, prep_phase, abort_flag);
-            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
-            prep_phase ^= 1;
-            mma_pending = false;
+            gram_waited = c;
             tc_fence_after();
 
-            // ---- A (fp32, lanes 0..63) and P (bf16, lanes 64..127); 32 columns per thread
+            // ---- P (bf16, lanes 0..63) and A (fp32, lanes 64..127); 32 columns per thread
             {
-                const bool is_a = L < 64;
-                const int r = is_a ? L : L - 64;
+                const bool is_a = L >= 64;
+                const int r = is_a ? L - 64 : L;
                 const int j0 = hh * 32;
                 float x[32];
                 tmem_ld32(trow + COL_G + j0, x);
@@ -491,21 +508,46 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 store_t12_frag(t12, sBet, sGam, 32 + 16 * mt, 8 * nt, g, t, y, -1.f);
             }
+            // ---- R_D[s] is free once the chain has read chunk c - 2's output from it;
+            //      zero its output half (the chain's products accumulate onto it)
+            if (c >= 2) fail = !mbar_wait_or_abort(&bars->dfree[s], ((c - 2) >> 1) & 1, abort_flag);
+            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
+            tc_fence_after();
+            {
+                float z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = 0.f;
+                tmem_st32(trow + COL_D + 128 * s + 64 + 32 * hh, z);
+                tmem_wait_st();
+            }
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_PREP, kPrep);
             // ---- U^T = V^T (T diag beta)^T,  W^T = K^T (T diag beta gamma)^T
-            if (pt == 0) {
+            if (pt == 64) {
                 tc_fence_after();
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_U + 64 * s, make_sdesc(st_s + ST_V + kk * 2048, 8192, 1024),
+                    mma_bf16(tmem + COL_D + 128 * s, make_sdesc(st_s + ST_VW0 + kk * 2048, ST_HALF, 1024),
                              make_sdesc(sbase + OFF_T12 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_W, make_sdesc(st_s + ST_K0 + kk * 2048, 16384, 1024),
+                    mma_bf16(tmem + COL_W, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
                              make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
                 mma_commit(&bars->prep_mma);
+                // the next chunk's Gram product, as soon as its inputs have landed (R_G has
+                // been read); a failed wait has set the abort flag
+                if (c + 1 < n_chunks && mbar_wait_or_abort(&bars->full[s ^ 1], ((c + 1) >> 1) & 1, abort_flag)) {
+                    issue_gram(c + 1);
+                    gram_issued = c + 1;
+                }
+            }
+            // the next chunk's decays (nobody reads this chunk's G, gamma, beta any more)
+            if (pt < 64 && c + 1 < n_chunks) {
+                scan_decays(c + 1, g_next, b_next);
+                const int tn = (c + 2) * kC + pt;
+                g_next = (tn < S) ? g_log[(size_t)bh * S + tn] : 0.f;
+                b_next = (tn < S) ? beta[(size_t)bh * S + tn] : 0.f;
             }
             mma_pending = true;
             fail = !mbar_wait_or_abort(&bars->prep_mma, prep_phase, abort_flag);
@@ -513,18 +555,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             prep_phase ^= 1;
             mma_pending = false;
             tc_fence_after();
-            // ---- -W over V (the U product has read V): row dk = L, 32 token columns
+            // ---- -W over V (the U product has read V), K-major: thread (dk = L, tokens
+            //      32 hh ..) writes column L % 64 of box L / 64, rows 32 hh .. 32 hh + 31
             {
                 float x[32];
                 tmem_ld32(trow + COL_W + hh * 32, x);
                 tmem_wait_ld();
-                st_row_bf16x32(st + ST_V, L, hh * 64, x, -1.f);
+                uint8_t* box = st + ((L >> 6) ? ST_VW1 : ST_VW0);
+                const uint32_t cb = 2u * (uint32_t)(L & 63);
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(32 * hh + i, cb)) = __float2bfloat16_rn(-x[i]);
             }
             fence_proxy_async_smem();
             tc_fence_before();
             mbar_arrive(&bars->ready[s]);
         }
-        if (mma_pending) (void)mbar_wait(&bars->prep_mma, prep_phase);
+        if (pt == 64) {  // drain what this thread issued (a completed phase returns at once)
+            if (mma_pending) (void)mbar_wait(&bars->prep_mma, prep_phase);
+            if (gram_issued > gram_waited) (void)mbar_wait(&bars->gram, gram_issued & 1);
+        }
     } else {
         // ------------------------------------------------------------ chain
         const int ct = tid - kPrep;  // dv row = TMEM lane
@@ -562,28 +612,23 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t st_s = sbase + s * STAGE_BYTES;
             bool fail = !mbar_wait_or_abort(&bars->ready[s], (c >> 1) & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
-            const float gC = sGC[s];
+            const float gC = sGC[c % 3];
+            const float ec_row = sEcs[64 * (c % 3) + (ct >> 1)];
             tc_fence_after();
             if (ct == 0) {
-                // Delta^T = U^T + S0^T (-W)^T
+                // [Delta^T | O^T] += S0^T [-W; Q']^T: Delta^T = U^T - S0^T W^T, O^T = S0^T Q'^T
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + COL_U + 64 * s,
+                    mma_bf16(tmem + COL_D + 128 * s,
                              make_sdesc(sbase + OFF_SB + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                             make_sdesc(st_s + ST_V + kk * 2048, 8192, 1024), IDESC_N64_KM, 1);
+                             make_sdesc(st_s + ST_VW0 + (kk >> 2) * ST_HALF + (kk & 3) * 32, 16, 1024),
+                             IDESC_N128_KK, 1);
                 mma_commit(&bars->c1);
-                // O^T = S0^T Q'^T (first part of the output)
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint32_t off = (kk >> 2) * 16384 + (kk & 3) * 32;
-                    mma_bf16(tmem + COL_O + 64 * s, make_sdesc(sbase + OFF_SB + off, 16, 1024),
-                             make_sdesc(st_s + ST_Q0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
-                }
             }
             issued1 = c;
             // K~ = diag(exp(G_C - G)) K in place while the products run (prep's W product has
             // read K; the state increment below reads K~): row ct / 2 of box ct % 2
-            scale_row_chunks<8>(sm + s * STAGE_BYTES + ((ct & 1) ? ST_K1 : ST_K0), ct >> 1, 0, sEcs[64 * s + (ct >> 1)]);
+            scale_row_chunks<8>(sm + s * STAGE_BYTES + ((ct & 1) ? ST_K1 : ST_K0), ct >> 1, 0, ec_row);
             // S^T <- gamma_C S^T in TMEM while the products run; the increment accumulates onto it
 #pragma unroll 1
             for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -600,10 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_after();
             {
                 float x[32];
-                tmem_ld32(trow + COL_U + 64 * s, x);
+                tmem_ld32(trow + COL_D + 128 * s, x);
                 tmem_wait_ld();
                 st_row_bf16x32(sm + OFF_DT, ct, 0, x);
-                tmem_ld32(trow + COL_U + 64 * s + 32, x);
+                tmem_ld32(trow + COL_D + 128 * s + 32, x);
                 tmem_wait_ld();
                 st_row_bf16x32(sm + OFF_DT, ct, 64, x);
             }
@@ -617,18 +662,22 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
                     mma_bf16(tmem + COL_S, make_sdesc(sbase + OFF_DT + kk * 32, 16, 1024),
-                             make_sdesc(st_s + ST_K0 + kk * 2048, 16384, 1024), IDESC_N128_KM, 1);
+                             make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024), IDESC_N128_KM, 1);
                 mma_commit(&bars->c2);
                 // O^T += Delta^T P^T
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_O + 64 * s, make_sdesc(sbase + OFF_DT + kk * 32, 16, 1024),
+                    mma_bf16(tmem + COL_D + 128 * s + 64, make_sdesc(sbase + OFF_DT + kk * 32, 16, 1024),
                              make_sdesc(st_s + ST_P + kk * 32, 16, 1024), IDESC_N64_KK, 1);
                 mma_commit(&bars->c3);
             }
             issued23 = c;
             // output of the previous chunk (its accumulator completed last iteration)
-            if (c >= 1) write_out_tile(sm + OFF_OUT, trow + COL_O + 64 * ((c - 1) & 1), ct, scale);
+            if (c >= 1) {
+                write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * ((c - 1) & 1) + 64, ct, scale);
+                tc_fence_before();
+                mbar_arrive(&bars->dfree[(c - 1) & 1]);  // prep may rewrite R_D of chunk c - 1
+            }
             fail = !mbar_wait_or_abort(&bars->c2, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             tc_fence_after();
@@ -667,7 +716,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)mbar_wait(&bars->c3, c & 1);  // completed already (waited for inside the loop)
             }
             named_bar_sync(BAR_CHAIN, kChain);
-            write_out_tile(sm + OFF_OUT, trow + COL_O + 64 * (c & 1), ct, scale);
+            write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * (c & 1) + 64, ct, scale);
             fence_proxy_async_smem();
             named_bar_sync(BAR_CHAIN, kChain);
             if (ct == 0) {
