@@ -92,9 +92,35 @@ def recorded_traffic(kernel: str):
     return None
 
 
+# ------------------------------------------------------------------ ranks
+def rank_workload(w, rank: int):
+    """Each rank runs its own copy of the workload with its own seed: the
+    sequences are independent, so ranks never exchange data (weak scaling)."""
+    return w.with_(seed=w.seed + 1000 * rank)
+
+
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank time over all ranks (the only cross-rank operation
+    besides barriers)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device if device is not None else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def weak_scaling_value(tokens_per_rank: int, world: int, ms_per_step: float) -> float:
+    """Whole-job throughput: tokens of all ranks over the slowest rank's time."""
+    return tokens_per_rank * world / (ms_per_step * 1e-3)
+
+
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 20 ms; `summary` keeps those taken between
+    `mark_start()` and `mark_end()` (the timed region)."""
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -107,12 +133,18 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.FIELDS,
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
         time.sleep(0.3)
         return self
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_end(self):
+        self.t_end = time.time()
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -126,18 +158,27 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        import datetime
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        t0 = getattr(self, "t_start", 0.0) - 0.05
+        t1 = getattr(self, "t_end", 1e30) + 0.05
         for line in open(self.path):
             p = [x.strip() for x in line.split(",")]
-            if len(p) < 9:
+            if len(p) < 10:
                 continue
             try:
-                sm.append(float(p[1]))
-                mx.append(float(p[2]))
+                ts = datetime.datetime.strptime(p[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+            except ValueError:
+                ts = None
+            if ts is not None and not (t0 <= ts <= t1):
+                continue
+            try:
+                sm.append(float(p[2]))
+                mx.append(float(p[3]))
             except ValueError:
                 continue
-            for n, val in zip(names, p[5:9]):
+            for n, val in zip(names, p[6:10]):
                 if val.lower() == "active":
                     reasons.add(n)
         os.unlink(self.path)
@@ -190,7 +231,7 @@ def run_ours(args, rank, world, local_rank):
             dist.barrier()
 
     # ---------------- prefill, inputs resident in HBM
-    w = PREFILL.with_(seed=PREFILL.seed + 1000 * rank)
+    w = rank_workload(PREFILL, rank)
     x = workloads.make_inputs(w, device=dev)
     state = x["state"].clone()
     out = torch.empty((w.B, w.Hv, w.S, w.Dv), dtype=w.torch_dtype, device=dev)
@@ -208,21 +249,20 @@ def run_ours(args, rank, world, local_rank):
     with ClockSampler(local_rank) as clk:
         barrier()
         torch.cuda.synchronize()
+        clk.mark_start()
         for i in range(args.steps):
             ev[i][0].record(stream)
             prefill_step()
             ev[i][1].record(stream)
         torch.cuda.synchronize()
+        clk.mark_end()
         barrier()
     clocks = clk.summary()
     launch_ms = [a.elapsed_time(b) for a, b in ev]
     total_ms = ev[0][0].elapsed_time(ev[-1][1])
     ms_per_step = total_ms / args.steps
-    if world > 1:
-        t = torch.tensor([ms_per_step], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_per_step = float(t.item())
-    value = w.B * w.S * world / (ms_per_step * 1e-3)
+    ms_per_step = max_over_ranks(ms_per_step, world, dev)
+    value = weak_scaling_value(w.B * w.S, world, ms_per_step)
     avg_launch_s = statistics.mean(launch_ms) * 1e-3
     pbytes = prefill_bytes(w)
     pflops = prefill_flops(w)
@@ -235,7 +275,7 @@ def run_ours(args, rank, world, local_rank):
                        "algorithmic_flops_per_launch": pflops}}
 
     # ---------------- decode step, L2 flushed between launches
-    wd = DECODE.with_(seed=DECODE.seed + 1000 * rank)
+    wd = rank_workload(DECODE, rank)
     xd = workloads.make_inputs(wd, device=dev)
     dstate = xd["state"].clone()
     dout = torch.empty((wd.B, wd.Hv, 1, wd.Dv), dtype=wd.torch_dtype, device=dev)
@@ -297,11 +337,8 @@ def run_ours(args, rank, world, local_rank):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": w.B * w.S * world / (e2e_ms * 1e-3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    e2e = {"value": weak_scaling_value(w.B * w.S, world, e2e_ms), "unit": "tokens/s", "ms_per_step": e2e_ms,
            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     if gdn.device_status(local_rank) != 0:
         raise RuntimeError("a kernel reported a wait timeout")
@@ -360,7 +397,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--oracle-sequences", type=int, default=32)
