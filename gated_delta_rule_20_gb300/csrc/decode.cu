@@ -17,7 +17,8 @@
 // state (columns evolve independently: column c of S' depends only on column c
 // of S).  128 threads = 16 column groups of 4 floats x 8 row groups; thread
 // (rg, cg) holds rows rg, rg + 8, ... of its 4 columns.  A warp therefore reads
-// two full 256-byte row segments per load instruction.
+// two full 256-byte row segments per load instruction.  Four CTAs share an SM
+// (128 registers per thread), so that more state loads are in flight.
 #include <cuda_bf16.h>
 
 #include "gdn_internal.h"
@@ -45,7 +46,7 @@ template <>
 __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 template <typename T, bool kVec>
-__global__ void __launch_bounds__(kThreads) gdn_decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
+__global__ void __launch_bounds__(kThreads, 4) gdn_decode_kernel(const T* __restrict__ q, const T* __restrict__ k,
                                                               const T* __restrict__ v,
                                                               const float* __restrict__ g_log,
                                                               const float* __restrict__ beta, float scale,

@@ -21,7 +21,8 @@
 // head dimension (Dv or Dk = 128) on the M / TMEM-lane axis and the chunk's 64
 // tokens on N:
 //     R_G    = [Q; K] K^T       (lanes 0..63: Q K^T rows, 64..127: K K^T rows)
-//     R_D[s] = [V^T (T diag beta)^T | 0]          -> [U^T | 0]
+//     R_D[s] = [V^T (T diag beta)^T | 0]          -> [U^T | 0]   (the chain zeroes the
+//                                                   right half once it has read the output)
 //     R_W    = K^T (T diag beta gamma)^T         -> W^T
 //     R_D[s] += S0^T [-W; Q']^T  (one N = 128 product, chain)
 //                                                -> [Delta^T | S0^T Q'^T]
@@ -172,7 +173,6 @@ __device__ __forceinline__ void write_out_tile(uint8_t* tile, uint32_t taddr, in
 struct Bars {
     uint64_t full[2];   // TMA -> prep
     uint64_t ready[2];  // prep -> chain (kPrep arrivals)
-    uint64_t dfree[2];  // chain has read R_D[s] (its output) -> prep may rewrite it (kChain arrivals)
     uint64_t gram;      // prep: Gram product of a chunk done
     uint64_t prep_mma;  // prep: U, W products done
     uint64_t c1;        // chain: Delta product done
@@ -290,7 +290,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int s = 0; s < 2; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->ready[s], kPrep);
-            mbar_init(&bars->dfree[s], kChain);
         }
         mbar_init(&bars->gram, 1);
         mbar_init(&bars->prep_mma, 1);
@@ -364,12 +363,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             b_next = (kC + pt < S) ? beta[(size_t)bh * S + kC + pt] : 0.f;
             scan_decays(0, g0, b0);
         }
-        if (pt == 64 && n_chunks > 0) {
-            if (mbar_wait_or_abort(&bars->full[0], 0, abort_flag)) {
-                issue_gram(0);
-                gram_issued = 0;
-            }
-        }
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c & 1;
             const uint32_t st_s = sbase + s * STAGE_BYTES;
@@ -377,6 +370,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- chunk inputs have landed (the Gram product was issued at the end of the
             //      previous chunk; every thread still observes the load's completion)
             bool fail = !mbar_wait_or_abort(&bars->full[s], (c >> 1) & 1, abort_flag);
+            if (!fail && pt == 64 && gram_issued < c) {
+                issue_gram(c);
+                gram_issued = c;
+            }
             if (!fail) fail = !mbar_wait_or_abort(&bars->gram, c & 1, abort_flag);
             if (named_bar_any(BAR_PREP, kPrep, fail)) break;
             gram_waited = c;
@@ -508,18 +505,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 store_t12_frag(t12, sBet, sGam, 32 + 16 * mt, 8 * nt, g, t, y, -1.f);
             }
-            // ---- R_D[s] is free once the chain has read chunk c - 2's output from it;
-            //      zero its output half (the chain's products accumulate onto it)
-            if (c >= 2) fail = !mbar_wait_or_abort(&bars->dfree[s], ((c - 2) >> 1) & 1, abort_flag);
-            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
-            tc_fence_after();
-            {
-                float z[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) z[j] = 0.f;
-                tmem_st32(trow + COL_D + 128 * s + 64 + 32 * hh, z);
-                tmem_wait_st();
-            }
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_PREP, kPrep);
@@ -535,9 +520,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tmem + COL_W, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
                              make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
                 mma_commit(&bars->prep_mma);
-                // the next chunk's Gram product, as soon as its inputs have landed (R_G has
-                // been read); a failed wait has set the abort flag
-                if (c + 1 < n_chunks && mbar_wait_or_abort(&bars->full[s ^ 1], ((c + 1) >> 1) & 1, abort_flag)) {
+                // the next chunk's Gram product now if its inputs have already landed (R_G
+                // has been read); otherwise it is issued when the next chunk starts
+                if (c + 1 < n_chunks && mbar_try_wait(&bars->full[s ^ 1], ((c + 1) >> 1) & 1)) {
                     issue_gram(c + 1);
                     gram_issued = c + 1;
                 }
@@ -578,18 +563,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ chain
         const int ct = tid - kPrep;  // dv row = TMEM lane
-        {
-            const float* Sg = state + (size_t)bh * kD * kD;
-#pragma unroll 1
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                float x[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = zero_init ? 0.f : Sg[(size_t)(c0 + j) * kD + ct];
-                tmem_st32(trow + COL_S + c0, x);
-                st_row_bf16x32(sm + OFF_SB + (c0 >> 6) * 16384, ct, (c0 & 63) * 2, x);
-            }
-            tmem_wait_st();
-        }
+        // the first two chunks' loads go out before anything else
         int last_load[2] = {-1, -1};  // last chunk loaded into each stage (thread ct == 32 loads)
         if (ct == 32) {
             tma_prefetch_desc(&tm_q);
@@ -601,6 +575,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                 last_load[c] = c;
             }
             if (n_chunks > 2) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, 2, bhk, bh);
+        }
+        {
+            const float* Sg = state + (size_t)bh * kD * kD;
+#pragma unroll 1
+            for (int c0 = 0; c0 < kD; c0 += 32) {
+                float x[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) x[j] = zero_init ? 0.f : Sg[(size_t)(c0 + j) * kD + ct];
+                tmem_st32(trow + COL_S + c0, x);
+                st_row_bf16x32(sm + OFF_SB + (c0 >> 6) * 16384, ct, (c0 & 63) * 2, x);
+            }
+            // both output accumulators start at zero (the chain's products accumulate onto them)
+            float z[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) z[j] = 0.f;
+#pragma unroll
+            for (int st = 0; st < 2; ++st) {
+                tmem_st32(trow + COL_D + 128 * st + 64, z);
+                tmem_st32(trow + COL_D + 128 * st + 96, z);
+            }
+            tmem_wait_st();
         }
         fence_proxy_async_smem();
         tc_fence_before();
@@ -674,9 +669,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             issued23 = c;
             // output of the previous chunk (its accumulator completed last iteration)
             if (c >= 1) {
-                write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * ((c - 1) & 1) + 64, ct, scale);
-                tc_fence_before();
-                mbar_arrive(&bars->dfree[(c - 1) & 1]);  // prep may rewrite R_D of chunk c - 1
+                // the output of chunk c - 1, then zero that accumulator for chunk c + 1
+                const uint32_t o_addr = trow + COL_D + 128 * ((c - 1) & 1) + 64;
+                write_out_tile(sm + OFF_OUT, o_addr, ct, scale);
+                float z[32];
+#pragma unroll
+                for (int j = 0; j < 32; ++j) z[j] = 0.f;
+                tmem_st32(o_addr, z);
+                tmem_st32(o_addr + 32, z);
+                tmem_wait_st();  // ordered before the next product on this accumulator by the barriers below
             }
             fail = !mbar_wait_or_abort(&bars->c2, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
@@ -796,9 +797,20 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
         !encode_bf16_3d(&tv, p.v, p.B * p.Hv, p.S, 64, true) ||
         !encode_bf16_3d(&to, p.out, p.B * p.Hv, p.S, 128, false))
         return GDN_ERR_CUDA;
-    if (cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)SMEM_ALLOC) != cudaSuccess)
-        return GDN_ERR_CUDA;
+    // the shared-memory opt-in is set once per device
+    static std::mutex mu;
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GDN_ERR_CUDA;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        if (!configured[dev]) {
+            if (cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_ALLOC) != cudaSuccess)
+                return GDN_ERR_CUDA;
+            configured[dev] = true;
+        }
+    }
     gdn_prefill_tc_kernel<<<p.B * p.Hv, kThreads, SMEM_ALLOC, stream>>>(
         tq, tk, tv, to, p.g_log, p.beta, p.state, p.scale, p.Hk, p.Hv, p.S, p.zero_init ? 1 : 0, status_word);
     return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
