@@ -71,17 +71,18 @@ constexpr int kChain = 128;
 constexpr int kThreads = kPrep + kChain;
 constexpr uint32_t kTmemCols = 512;
 
-// TMEM columns (fp32, 128 lanes each)
-constexpr uint32_t COL_G = 0;    // 64: Gram
-constexpr uint32_t COL_W = 64;   // 64: W^T
-constexpr uint32_t COL_D = 128;  // 2 x 128, per stage: [U^T -> Delta^T | output accumulator]
-constexpr uint32_t COL_S = 384;  // 128: the fp32 state S^T (lane dv, column dk)
+// TMEM columns (32-bit, 128 lanes each)
+constexpr uint32_t COL_G = 0;     // 64: Gram
+constexpr uint32_t COL_D = 64;    // 2 x 128, chunk c in buffer c % 2: [U^T -> Delta^T | W^T, then output]
+constexpr uint32_t COL_S = 320;   // 128: the fp32 state S^T (lane dv, column dk)
+constexpr uint32_t COL_SA = 448;  // 64: the state as bf16 pairs, the A operand of the chunk's first product
 
 // Shared memory (bytes from a 1024-aligned base).  bf16 tiles: rows of 128 B
 // with the 128-byte swizzle.
 // Stage: per 64-wide half h of the head dims, three [64 tokens][64] boxes
 // [V (dv half h), later -W (dk half h, K-major) | Q | K], then P.  [-W; Q'] and
 // [Q; K] are each one contiguous 128-row K-major operand.
+constexpr int kStages = 3;
 constexpr uint32_t STAGE_BYTES = 57344;
 constexpr uint32_t ST_HALF = 24576;  // distance between the two halves
 constexpr uint32_t ST_VW0 = 0;       // V dv 0..63, then -W [64 r][dk 0..63]
@@ -91,27 +92,21 @@ constexpr uint32_t ST_VW1 = ST_VW0 + ST_HALF;
 constexpr uint32_t ST_Q1 = ST_Q0 + ST_HALF;
 constexpr uint32_t ST_K1 = ST_K0 + ST_HALF;
 constexpr uint32_t ST_P = 49152;     // P [64 r][64 j]
+constexpr uint32_t ST_DT = 0;        // Delta^T [128 dv][64 j] K-major, over -W and Q' once the first product is done
 constexpr uint32_t LOAD_BYTES = 49152;
-constexpr uint32_t OFF_T12 = 2 * STAGE_BYTES;  // T diag(beta), T diag(beta gamma): [64 r][64 j] bf16 each
-constexpr uint32_t OFF_AT = OFF_T12 + 16384;   // fp32 A, solved in place into T: [64][68]
-constexpr int AT_STRIDE = 68;
-constexpr uint32_t OFF_SB = OFF_AT + 17408;    // S^T bf16 [dv][dk]: dk halves at +0, +16384
-constexpr uint32_t OFF_DT = OFF_SB + 32768;    // Delta^T bf16 [dv][64 j]
-constexpr uint32_t OFF_OUT = OFF_DT + 16384;   // out tile [64 r][128 dv] bf16, unswizzled
-constexpr uint32_t OFF_SCR = OFF_OUT + 16384;   // solve scratch (fp32 X tiles)
-constexpr uint32_t OFF_SMALL = OFF_SCR + 8192;
+constexpr uint32_t OFF_T12 = kStages * STAGE_BYTES;  // T diag(beta), T diag(beta gamma): [64 r][64 j] bf16 each
+constexpr uint32_t OFF_AT = OFF_T12 + 16384;   // fp32 A, solved in place into T: [64][68]; its upper-right
+constexpr int AT_STRIDE = 68;                  // 32 x 32 quadrant (never read as T) is the solve's scratch
+constexpr uint32_t OFF_OUT = OFF_AT + 17408;   // out tile [64 r][128 dv] bf16, unswizzled
+constexpr uint32_t OFF_SMALL = OFF_OUT + 16384;
 // small area (floats): G2[64] = log2(e) x cumulative log-decay, gam[64], bet[64],
-// then per chunk c in slot c % 3 (written one chunk ahead, read by the chain):
-// ec[3][64] = exp(G_C - G), gC[3] = exp(G_C)
-constexpr uint32_t OFF_BAR = OFF_SMALL + 1792;
+// then per chunk c in slot c % 4 (written up to three chunks ahead of the chain):
+// ec[4][64] = exp(G_C - G), gC[4] = exp(G_C)
+constexpr uint32_t OFF_BAR = OFF_SMALL + 2048;
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
-static_assert(OFF_SB % 1024 == 0 && OFF_DT % 1024 == 0 && OFF_OUT % 1024 == 0, "tile alignment");
+static_assert(OFF_T12 % 1024 == 0 && OFF_OUT % 1024 == 0, "tile alignment");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
-// solve scratch
-constexpr uint32_t SCR_X1 = 0;     // level 1: 4 tiles of 16 x 8 fp32 (stride 8)
-constexpr uint32_t SCR_X2 = 2048;  // level 2: 32 x 32 fp32 (stride 40)
-constexpr int X2_STRIDE = 40;
 
 constexpr uint32_t IDESC_N64_KK = make_idesc_bf16(128, 64, 0, 0);
 constexpr uint32_t IDESC_N64_MK = make_idesc_bf16(128, 64, 1, 0);   // A MN-major
@@ -171,8 +166,9 @@ __device__ __forceinline__ void write_out_tile(uint8_t* tile, uint32_t taddr, in
 }
 
 struct Bars {
-    uint64_t full[2];   // TMA -> prep
-    uint64_t ready[2];  // prep -> chain (kPrep arrivals)
+    uint64_t full[kStages];   // TMA -> prep
+    uint64_t ready[kStages];  // prep -> chain (kPrep arrivals)
+    uint64_t dfree[2];        // chain has read buffer R_D[b]'s output -> prep may reuse it (kChain arrivals)
     uint64_t gram;      // prep: Gram product of a chunk done
     uint64_t prep_mma;  // prep: U, W products done
     uint64_t c1;        // chain: Delta product done
@@ -273,8 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* sG = reinterpret_cast<float*>(sm + OFF_SMALL);
     float* sGam = sG + 64;
     float* sBet = sG + 128;
-    float* sEcs = sG + 192;  // [3][64], slot c % 3
-    float* sGC = sG + 384;   // [3], slot c % 3
+    float* sEcs = sG + 192;  // [4][64], slot c % 4
+    float* sGC = sG + 448;   // [4], slot c % 4
     volatile int* abort_flag = &bars->abort;
 
     const int tid = threadIdx.x;
@@ -287,10 +283,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_chunks = (S + kC - 1) / kC;
 
     if (tid == 0) {
-        for (int s = 0; s < 2; ++s) {
+        for (int s = 0; s < kStages; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->ready[s], kPrep);
         }
+        for (int b = 0; b < 2; ++b) mbar_init(&bars->dfree[b], kChain);
         mbar_init(&bars->gram, 1);
         mbar_init(&bars->prep_mma, 1);
         mbar_init(&bars->c1, 1);
@@ -317,15 +314,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int hh = warp >> 2;              // column half (32 columns) of the 64-wide products
         const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
         float* M = reinterpret_cast<float*>(sm + OFF_AT);
-        float* X1 = reinterpret_cast<float*>(sm + OFF_SCR + SCR_X1);
-        float* X2 = reinterpret_cast<float*>(sm + OFF_SCR + SCR_X2);
         uint8_t* t12 = sm + OFF_T12;
         uint32_t prep_phase = 0;
         bool mma_pending = false;
         int gram_issued = -1, gram_waited = -1;
         // Gram product [Q; K] K^T of chunk cc into R_G (issued by thread 64 once the chunk has landed)
         auto issue_gram = [&](int cc) {
-            const uint32_t st_c = sbase + (cc & 1) * STAGE_BYTES;
+            const uint32_t st_c = sbase + (cc % kStages) * STAGE_BYTES;
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
@@ -351,8 +346,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             sG[pt] = G * kLog2e;
             sGam[pt] = exp2_approx(G * kLog2e);
             sBet[pt] = bv;
-            sEcs[64 * (cc % 3) + pt] = exp2_approx((GC - G) * kLog2e);
-            if (pt == 0) sGC[cc % 3] = exp2_approx(GC * kLog2e);
+            sEcs[64 * (cc & 3) + pt] = exp2_approx((GC - G) * kLog2e);
+            if (pt == 0) sGC[cc & 3] = exp2_approx(GC * kLog2e);
         };
         // decay inputs: chunk 0 now, chunk 1 prefetched (threads 0..63)
         float g_next = 0.f, b_next = 0.f;
@@ -364,12 +359,13 @@ __global__ void __launch_bounds__(kThreads, 1)
             scan_decays(0, g0, b0);
         }
         for (int c = 0; c < n_chunks; ++c) {
-            const int s = c & 1;
+            const int s = c % kStages;  // input stage
+            const int db = c & 1;       // TMEM buffer R_D
             const uint32_t st_s = sbase + s * STAGE_BYTES;
             uint8_t* st = sm + s * STAGE_BYTES;
             // ---- chunk inputs have landed (the Gram product was issued at the end of the
             //      previous chunk; every thread still observes the load's completion)
-            bool fail = !mbar_wait_or_abort(&bars->full[s], (c >> 1) & 1, abort_flag);
+            bool fail = !mbar_wait_or_abort(&bars->full[s], (c / kStages) & 1, abort_flag);
             if (!fail && pt == 64 && gram_issued < c) {
                 issue_gram(c);
                 gram_issued = c;
@@ -425,7 +421,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // ---- level 1 (warps 0..3): T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22
                 const int blk = warp >> 1, nt = warp & 1;
                 const int rb = 32 * blk + 16, cb = 32 * blk;
-                float* xs = X1 + warp * 128;  // 16 x 8, stride 8
+                const int xc = 32 + 8 * warp;  // scratch tile: rows 0..15, columns xc .. xc + 7 of M
                 float d[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
@@ -435,14 +431,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     load_bfrag(M, AT_STRIDE, cb + 8 * ks, cb + 8 * nt, g, t, bf);
                     mma_tf32_16x8x8(d, a, bf);
                 }
-                store_cfrag(xs, 8, 0, 0, g, t, d, 1.f);
+                store_cfrag(M, AT_STRIDE, 0, xc, g, t, d, 1.f);
                 named_bar_sync(BAR_L1, 128);  // every X tile is out of A's block before T overwrites it
                 float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int ks = 0; ks < 2; ++ks) {
                     uint32_t a[4], bf[2];
                     load_afrag(M, AT_STRIDE, rb, rb + 8 * ks, g, t, a);
-                    load_bfrag(xs, 8, 8 * ks, 0, g, t, bf);
+                    load_bfrag(M, AT_STRIDE, 8 * ks, xc, g, t, bf);
                     mma_tf32_16x8x8(y, a, bf);
                 }
                 store_cfrag(M, AT_STRIDE, rb, cb + 8 * nt, g, t, y, -1.f);
@@ -492,7 +488,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     load_bfrag(M, AT_STRIDE, 8 * ks, 8 * nt, g, t, bf);
                     mma_tf32_16x8x8(d, a, bf);
                 }
-                store_cfrag(X2, X2_STRIDE, 16 * mt, 8 * nt, g, t, d, 1.f);
+                store_cfrag(M, AT_STRIDE, 16 * mt, 32 + 8 * nt, g, t, d, 1.f);  // scratch: upper-right quadrant
                 named_bar_sync(BAR_PREP, kPrep);
                 float y[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -500,7 +496,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (ks >= 2 * mt + 2) continue;  // T[32:64, 32:64] is lower triangular
                     uint32_t a[4], bf[2];
                     load_afrag(M, AT_STRIDE, 32 + 16 * mt, 32 + 8 * ks, g, t, a);
-                    load_bfrag(X2, X2_STRIDE, 8 * ks, 8 * nt, g, t, bf);
+                    load_bfrag(M, AT_STRIDE, 8 * ks, 32 + 8 * nt, g, t, bf);
                     mma_tf32_16x8x8(y, a, bf);
                 }
                 store_t12_frag(t12, sBet, sGam, 32 + 16 * mt, 8 * nt, g, t, y, -1.f);
@@ -508,21 +504,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_PREP, kPrep);
-            // ---- U^T = V^T (T diag beta)^T,  W^T = K^T (T diag beta gamma)^T
+            // ---- [U^T | W^T] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T] into R_D[db],
+            //      once the chain has read chunk c - 2's output from that buffer
             if (pt == 64) {
+                const bool free_ok = (c < 2) || mbar_wait_or_abort(&bars->dfree[db], ((c - 2) >> 1) & 1, abort_flag);
                 tc_fence_after();
+                if (free_ok) {
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_D + 128 * s, make_sdesc(st_s + ST_VW0 + kk * 2048, ST_HALF, 1024),
-                             make_sdesc(sbase + OFF_T12 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_D + 128 * db, make_sdesc(st_s + ST_VW0 + kk * 2048, ST_HALF, 1024),
+                                 make_sdesc(sbase + OFF_T12 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
 #pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_W, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
-                             make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
-                mma_commit(&bars->prep_mma);
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
+                                 make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+                    mma_commit(&bars->prep_mma);
+                }
                 // the next chunk's Gram product now if its inputs have already landed (R_G
                 // has been read); otherwise it is issued when the next chunk starts
-                if (c + 1 < n_chunks && mbar_try_wait(&bars->full[s ^ 1], ((c + 1) >> 1) & 1)) {
+                if (free_ok && c + 1 < n_chunks &&
+                    mbar_try_wait(&bars->full[(c + 1) % kStages], ((c + 1) / kStages) & 1)) {
                     issue_gram(c + 1);
                     gram_issued = c + 1;
                 }
@@ -541,16 +542,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_pending = false;
             tc_fence_after();
             // ---- -W over V (the U product has read V), K-major: thread (dk = L, tokens
-            //      32 hh ..) writes column L % 64 of box L / 64, rows 32 hh .. 32 hh + 31
+            //      32 hh ..) writes column L % 64 of box L / 64, rows 32 hh .. 32 hh + 31;
+            //      then the output half of R_D[db] is zeroed for the chain's accumulation
             {
                 float x[32];
-                tmem_ld32(trow + COL_W + hh * 32, x);
+                const uint32_t waddr = trow + COL_D + 128 * db + 64 + hh * 32;
+                tmem_ld32(waddr, x);
                 tmem_wait_ld();
                 uint8_t* box = st + ((L >> 6) ? ST_VW1 : ST_VW0);
                 const uint32_t cb = 2u * (uint32_t)(L & 63);
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                     *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(32 * hh + i, cb)) = __float2bfloat16_rn(-x[i]);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) x[i] = 0.f;
+                tmem_st32(waddr, x);
+                tmem_wait_st();
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -563,67 +570,69 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ------------------------------------------------------------ chain
         const int ct = tid - kPrep;  // dv row = TMEM lane
-        // the first two chunks' loads go out before anything else
-        int last_load[2] = {-1, -1};  // last chunk loaded into each stage (thread ct == 32 loads)
+        // the first chunks' loads go out before anything else
+        int last_load[kStages];  // last chunk loaded into each stage (thread ct == 32 loads)
+#pragma unroll
+        for (int i = 0; i < kStages; ++i) last_load[i] = -1;
         if (ct == 32) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_o);
-            for (int c = 0; c < 2 && c < n_chunks; ++c) {
+            for (int c = 0; c < kStages && c < n_chunks; ++c) {
                 load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, c, bhk, bh);
                 last_load[c] = c;
             }
-            if (n_chunks > 2) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, 2, bhk, bh);
+            if (n_chunks > kStages) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, kStages, bhk, bh);
         }
+        // S^T (fp32) and its bf16 copy (the A operand of each chunk's first product) into TMEM
+        auto store_state_bf16 = [&](int half, const float* x64) {
+            uint32_t u[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) u[j] = pack_bf16x2(x64[2 * j], x64[2 * j + 1]);
+            tmem_st32u(trow + COL_SA + 32 * half, u);
+        };
         {
             const float* Sg = state + (size_t)bh * kD * kD;
 #pragma unroll 1
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                float x[32];
+            for (int h64 = 0; h64 < 2; ++h64) {
+                float x[64];
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] = zero_init ? 0.f : Sg[(size_t)(c0 + j) * kD + ct];
-                tmem_st32(trow + COL_S + c0, x);
-                st_row_bf16x32(sm + OFF_SB + (c0 >> 6) * 16384, ct, (c0 & 63) * 2, x);
-            }
-            // both output accumulators start at zero (the chain's products accumulate onto them)
-            float z[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) z[j] = 0.f;
-#pragma unroll
-            for (int st = 0; st < 2; ++st) {
-                tmem_st32(trow + COL_D + 128 * st + 64, z);
-                tmem_st32(trow + COL_D + 128 * st + 96, z);
+                for (int j = 0; j < 64; ++j) x[j] = zero_init ? 0.f : Sg[(size_t)(64 * h64 + j) * kD + ct];
+                tmem_st32(trow + COL_S + 64 * h64, *reinterpret_cast<const float(*)[32]>(x));
+                tmem_st32(trow + COL_S + 64 * h64 + 32, *reinterpret_cast<const float(*)[32]>(x + 32));
+                store_state_bf16(h64, x);
             }
             tmem_wait_st();
         }
-        fence_proxy_async_smem();
         tc_fence_before();
         named_bar_sync(BAR_CHAIN, kChain);
         int issued1 = -1, issued23 = -1;  // last chunk whose chain MMAs were committed
         bool ok = true;
         for (int c = 0; c < n_chunks && ok; ++c) {
-            const int s = c & 1;
+            const int s = c % kStages;  // input stage
+            const int db = c & 1;       // TMEM buffer R_D
             const uint32_t st_s = sbase + s * STAGE_BYTES;
-            bool fail = !mbar_wait_or_abort(&bars->ready[s], (c >> 1) & 1, abort_flag);
+            uint8_t* st = sm + s * STAGE_BYTES;
+            bool fail = !mbar_wait_or_abort(&bars->ready[s], (c / kStages) & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
-            const float gC = sGC[c % 3];
-            const float ec_row = sEcs[64 * (c % 3) + (ct >> 1)];
+            const float gC = sGC[c & 3];
+            const float ec_row = sEcs[64 * (c & 3) + (ct >> 1)];
             tc_fence_after();
             if (ct == 0) {
                 // [Delta^T | O^T] += S0^T [-W; Q']^T: Delta^T = U^T - S0^T W^T, O^T = S0^T Q'^T
+                // (A = the bf16 state in TMEM, 8 columns per 16-wide K step)
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + COL_D + 128 * s,
-                             make_sdesc(sbase + OFF_SB + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                             make_sdesc(st_s + ST_VW0 + (kk >> 2) * ST_HALF + (kk & 3) * 32, 16, 1024),
-                             IDESC_N128_KK, 1);
+                    mma_bf16_tmem_a(tmem + COL_D + 128 * db, tmem + COL_SA + 8 * kk,
+                                    make_sdesc(st_s + ST_VW0 + (kk >> 2) * ST_HALF + (kk & 3) * 32, 16, 1024),
+                                    IDESC_N128_KK, 1);
                 mma_commit(&bars->c1);
             }
             issued1 = c;
             // K~ = diag(exp(G_C - G)) K in place while the products run (prep's W product has
             // read K; the state increment below reads K~): row ct / 2 of box ct % 2
-            scale_row_chunks<8>(sm + s * STAGE_BYTES + ((ct & 1) ? ST_K1 : ST_K0), ct >> 1, 0, ec_row);
+            scale_row_chunks<8>(st + ((ct & 1) ? ST_K1 : ST_K0), ct >> 1, 0, ec_row);
             // S^T <- gamma_C S^T in TMEM while the products run; the increment accumulates onto it
 #pragma unroll 1
             for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -638,14 +647,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             fail = !mbar_wait_or_abort(&bars->c1, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             tc_fence_after();
+            // Delta^T as a K-major bf16 operand over -W and Q' (both consumed by the product above)
             {
                 float x[32];
-                tmem_ld32(trow + COL_D + 128 * s, x);
+                tmem_ld32(trow + COL_D + 128 * db, x);
                 tmem_wait_ld();
-                st_row_bf16x32(sm + OFF_DT, ct, 0, x);
-                tmem_ld32(trow + COL_D + 128 * s + 32, x);
+                st_row_bf16x32(st + ST_DT, ct, 0, x);
+                tmem_ld32(trow + COL_D + 128 * db + 32, x);
                 tmem_wait_ld();
-                st_row_bf16x32(sm + OFF_DT, ct, 64, x);
+                st_row_bf16x32(st + ST_DT, ct, 64, x);
             }
             fence_proxy_async_smem();
             tc_fence_before();
@@ -656,50 +666,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // S^T += Delta^T K~
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_S, make_sdesc(sbase + OFF_DT + kk * 32, 16, 1024),
+                    mma_bf16(tmem + COL_S, make_sdesc(st_s + ST_DT + kk * 32, 16, 1024),
                              make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024), IDESC_N128_KM, 1);
                 mma_commit(&bars->c2);
                 // O^T += Delta^T P^T
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_D + 128 * s + 64, make_sdesc(sbase + OFF_DT + kk * 32, 16, 1024),
+                    mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_DT + kk * 32, 16, 1024),
                              make_sdesc(st_s + ST_P + kk * 32, 16, 1024), IDESC_N64_KK, 1);
                 mma_commit(&bars->c3);
             }
             issued23 = c;
-            // output of the previous chunk (its accumulator completed last iteration)
+            // output of the previous chunk (its accumulator completed last iteration); prep may
+            // then reuse that buffer
             if (c >= 1) {
-                // the output of chunk c - 1, then zero that accumulator for chunk c + 1
-                const uint32_t o_addr = trow + COL_D + 128 * ((c - 1) & 1) + 64;
-                write_out_tile(sm + OFF_OUT, o_addr, ct, scale);
-                float z[32];
-#pragma unroll
-                for (int j = 0; j < 32; ++j) z[j] = 0.f;
-                tmem_st32(o_addr, z);
-                tmem_st32(o_addr + 32, z);
-                tmem_wait_st();  // ordered before the next product on this accumulator by the barriers below
+                write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * ((c - 1) & 1) + 64, ct, scale);
+                tc_fence_before();
+                mbar_arrive(&bars->dfree[(c - 1) & 1]);
             }
             fail = !mbar_wait_or_abort(&bars->c2, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             tc_fence_after();
             if (ct == 32) {
                 // once the output product has completed, every read of this stage is done:
-                // reload it with chunk c + 2 and prefetch chunk c + 3 into L2
+                // reload it with chunk c + kStages and prefetch the chunk after into L2
                 // (a failed wait has set the abort flag, which every role checks)
-                if (mbar_wait_or_abort(&bars->c3, c & 1, abort_flag) && c + 2 < n_chunks) {
-                    load_chunk(sm + s * STAGE_BYTES, &bars->full[s], &tm_q, &tm_k, &tm_v, c + 2, bhk, bh);
-                    last_load[s] = c + 2;
-                    if (c + 3 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, c + 3, bhk, bh);
+                if (mbar_wait_or_abort(&bars->c3, c & 1, abort_flag) && c + kStages < n_chunks) {
+                    load_chunk(st, &bars->full[s], &tm_q, &tm_k, &tm_v, c + kStages, bhk, bh);
+                    last_load[s] = c + kStages;
+                    if (c + kStages + 1 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, c + kStages + 1, bhk, bh);
                 }
             }
-            // bf16 copy of the new state for the next chunk's products
+            // bf16 copy of the new state for the next chunk's first product
 #pragma unroll 1
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                float x[32];
-                tmem_ld32(trow + COL_S + c0, x);
+            for (int h64 = 0; h64 < 2; ++h64) {
+                float x[64];
+                tmem_ld32(trow + COL_S + 64 * h64, *reinterpret_cast<float(*)[32]>(x));
+                tmem_ld32(trow + COL_S + 64 * h64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
                 tmem_wait_ld();
-                st_row_bf16x32(sm + OFF_SB + (c0 >> 6) * 16384, ct, (c0 & 63) * 2, x);
+                store_state_bf16(h64, x);
             }
+            tmem_wait_st();
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_CHAIN, kChain);
@@ -717,6 +724,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 (void)mbar_wait(&bars->c3, c & 1);  // completed already (waited for inside the loop)
             }
             named_bar_sync(BAR_CHAIN, kChain);
+            tc_fence_after();
             write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * (c & 1) + 64, ct, scale);
             fence_proxy_async_smem();
             named_bar_sync(BAR_CHAIN, kChain);
@@ -743,8 +751,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (ct == 32)
-                for (int st = 0; st < 2; ++st)
-                    if (last_load[st] >= 0) (void)mbar_wait(&bars->full[st], (last_load[st] >> 1) & 1);
+                for (int i = 0; i < kStages; ++i)
+                    if (last_load[i] >= 0) (void)mbar_wait(&bars->full[i], (last_load[i] / kStages) & 1);
         }
         if (ct == 0) tma_store_wait_all0();
     }
