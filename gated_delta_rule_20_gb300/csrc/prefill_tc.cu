@@ -14,32 +14,31 @@
 //     U = T diag(beta) V,  W = T diag(beta gamma) K,  Delta = U - W S0
 //     O = scale (Q' S0 + P Delta),  Q' = diag(gamma) Q,
 //         P[r][j] = exp(G_r - G_j) q_r.k_j (j <= r)
-//     S_end = gamma_C S0 + K~^T Delta,  K~ = diag(exp(G_C - G)) K
+//     S_end = gamma_C S0 + K^T diag(exp(G_C - G)) Delta
 // Only exponents <= 0 are ever evaluated, so strong decay cannot overflow.
 //
 // Orientation.  Every tensor-core product is issued with M = 128 by putting a
 // head dimension (Dv or Dk = 128) on the M / TMEM-lane axis and the chunk's 64
 // tokens on N:
 //     R_G    = [Q; K] K^T       (lanes 0..63: Q K^T rows, 64..127: K K^T rows)
-//     R_D[s] = [V^T (T diag beta)^T | 0]          -> [U^T | 0]   (the chain zeroes the
-//                                                   right half once it has read the output)
-//     R_W    = K^T (T diag beta gamma)^T         -> W^T
-//     R_D[s] += S0^T [-W; Q']^T  (one N = 128 product, chain)
-//                                                -> [Delta^T | S0^T Q'^T]
-//     R_D[s] right half += Delta^T P^T           -> O^T / scale (chain)
-//     R_S   += Delta^T K~                        -> state increment, S^T layout
+//     R_D[b] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T]  -> [U^T | W^T]  (prep)
+//     R_D[b] += S0^T [-W; Q']^T  (one N = 128 product; the chain has zeroed the
+//                                 right half after reading W^T) -> [Delta^T | S0^T Q'^T]
+//     R_D[b] right half += Delta^T P^T                          -> O^T / scale
+//     R_S   += (Delta^T diag(exp(G_C - G))) K                   -> state increment, S^T layout
 //
 // Roles (one CTA per (batch, value head), 384 threads):
-//   prep warps (0-7)  -- per chunk: decay scan, the Gram product, A and P,
-//       the triangular solve, U and W, and the in-place rewrites Q -> Q',
-//       V -> -W, K -> K~ inside the chunk's input stage.  Warp w reads TMEM
-//       lanes 32 (w % 4) .. + 31 and, for 64-column products, columns
-//       32 (w / 4) .. + 31.  Prep runs up to one chunk ahead of the chain.
-//   chain warps (8-11) -- the serial part: Delta, the state carry (fp32 S^T in
-//       TMEM, lane i = dv row i, scaled by gamma_C in place and incremented
-//       by the tensor core), the output and its TMA store.  Once the products
-//       of chunk c have completed, the chain reloads that chunk's input stage
-//       with chunk c + 2 (TMA) and prefetches chunk c + 3 into L2.
+//   prep warps (0-7)  -- per chunk: decay scan (one chunk ahead), the Gram
+//       product, A and P, Q -> Q' in place, the triangular solve, T diag(beta)
+//       and T diag(beta gamma) in bf16, and the U/W product, whose completion
+//       the chain waits for.  Warp w reads TMEM lanes 32 (w % 4) .. + 31 and,
+//       for 64-column products, columns 32 (w / 4) .. + 31.
+//   chain warps (8-11) -- the serial part, thread i on TMEM lane i: -W over V,
+//       Delta, the state carry (fp32 S^T in TMEM, scaled by gamma_C when its
+//       bf16 copy is taken and incremented by the tensor core), the output and
+//       its TMA store.  Once the products of chunk c have completed, the chain
+//       reloads that chunk's input stage with chunk c + 3 (TMA) and prefetches
+//       chunk c + 4 into L2.
 //
 // Triangular solve: (I + A)^-1 for the 64x64 strictly lower A, blocked in
 // 16x16: diagonal blocks by forward substitution in fp32, off-diagonal blocks
@@ -87,22 +86,27 @@ constexpr uint32_t STAGE_BYTES = 57344;
 constexpr uint32_t ST_HALF = 24576;  // distance between the two halves
 constexpr uint32_t ST_VW0 = 0;       // V dv 0..63, then -W [64 r][dk 0..63]
 constexpr uint32_t ST_Q0 = 8192;     // Q (-> Q'), dk 0..63
-constexpr uint32_t ST_K0 = 16384;    // K (-> K~), dk 0..63
+constexpr uint32_t ST_K0 = 16384;    // K, dk 0..63
 constexpr uint32_t ST_VW1 = ST_VW0 + ST_HALF;
 constexpr uint32_t ST_Q1 = ST_Q0 + ST_HALF;
 constexpr uint32_t ST_K1 = ST_K0 + ST_HALF;
 constexpr uint32_t ST_P = 49152;     // P [64 r][64 j]
-constexpr uint32_t ST_DT = 0;        // Delta^T [128 dv][64 j] K-major, over -W and Q' once the first product is done
+// Delta^T [128 dv][64 j] K-major bf16, and Delta^T diag(exp(G_C - G)) likewise: written over
+// [-W; Q'] (dk 0..63 and dk 64..127) once the chain's first product has read them
+constexpr uint32_t ST_DT = 0;
+constexpr uint32_t ST_DT2 = ST_HALF;
 constexpr uint32_t LOAD_BYTES = 49152;
 constexpr uint32_t OFF_T12 = kStages * STAGE_BYTES;  // T diag(beta), T diag(beta gamma): [64 r][64 j] bf16 each
 constexpr uint32_t OFF_AT = OFF_T12 + 16384;   // fp32 A, solved in place into T: [64][68]; its upper-right
 constexpr int AT_STRIDE = 68;                  // 32 x 32 quadrant (never read as T) is the solve's scratch
 constexpr uint32_t OFF_OUT = OFF_AT + 17408;   // out tile [64 r][128 dv] bf16, unswizzled
 constexpr uint32_t OFF_SMALL = OFF_OUT + 16384;
-// small area (floats): G2[64] = log2(e) x cumulative log-decay, gam[64], bet[64],
-// then per chunk c in slot c % 4 (written up to three chunks ahead of the chain):
-// ec[4][64] = exp(G_C - G), gC[4] = exp(G_C)
-constexpr uint32_t OFF_BAR = OFF_SMALL + 2048;
+// small area (floats), per chunk c in slot c % 2:  G2[2][64] = log2(e) x cumulative
+// log-decay, gam[2][64] = exp(G), bet[2][64];  in slot c % 4 (read by the chain up to three
+// chunks behind the prep): ec[4][64] = exp(G_C - G), gC[4] = exp(G_C);  from float 704 the
+// raw decay inputs (log-decay, beta) [2][2][64], slot c % 2, fetched asynchronously
+constexpr uint32_t SM_G = 0, SM_GAM = 128, SM_BET = 256, SM_EC = 384, SM_GC = 640, SM_GB = 704;
+constexpr uint32_t OFF_BAR = OFF_SMALL + 4096;
 constexpr uint32_t SMEM_USED = OFF_BAR + 128;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(OFF_T12 % 1024 == 0 && OFF_OUT % 1024 == 0, "tile alignment");
@@ -170,7 +174,7 @@ struct Bars {
     uint64_t ready[kStages];  // prep -> chain (kPrep arrivals)
     uint64_t dfree[2];        // chain has read buffer R_D[b]'s output -> prep may reuse it (kChain arrivals)
     uint64_t gram;      // prep: Gram product of a chunk done
-    uint64_t prep_mma;  // prep: U, W products done
+    uint64_t prep_mma[2];  // U, W products of chunk c done, slot c % 2 (waited by the chain and by prep)
     uint64_t c1;        // chain: Delta product done
     uint64_t c2;        // chain: state increment done
     uint64_t c3;        // chain: output accumulator done
@@ -211,17 +215,18 @@ __device__ __forceinline__ void store_t12_frag(uint8_t* t12, const float* bet, c
 }
 
 // Level 0: diagonal 16 x 16 block `blk` of T = (I + A)^-1 by forward
-// substitution, one column per lane (lanes 16..31 repeat lanes 0..15).
+// substitution, one column per lane (lanes 16..31 repeat lanes 0..15).  Column
+// oriented: once x[m] is final it is eliminated from every later row, so the
+// dependent chain is one FMA per row.
 __device__ __forceinline__ void solve_diag_block(float* M, int blk, int lane) {
     const int base = blk * 16, j = lane & 15;
     float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        const float* row = M + (base + i) * AT_STRIDE + base;
-        float acc = (i == j) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
 #pragma unroll
-        for (int m = 0; m < i; ++m) acc = fmaf(-row[m], x[m], acc);
-        x[i] = acc;
+    for (int m = 0; m < 15; ++m) {
+#pragma unroll
+        for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-M[(base + i) * AT_STRIDE + base + m], x[m], x[i]);
     }
     __syncwarp();
     if (lane < 16) {
@@ -266,11 +271,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
     Bars* bars = reinterpret_cast<Bars*>(sm + OFF_BAR);
-    float* sG = reinterpret_cast<float*>(sm + OFF_SMALL);
-    float* sGam = sG + 64;
-    float* sBet = sG + 128;
-    float* sEcs = sG + 192;  // [4][64], slot c % 4
-    float* sGC = sG + 448;   // [4], slot c % 4
+    float* const small = reinterpret_cast<float*>(sm + OFF_SMALL);
+    float* sG = small + SM_G;      // [2][64], slot c % 2
+    float* sGam = small + SM_GAM;  // [2][64], slot c % 2
+    float* sBet = small + SM_BET;  // [2][64], slot c % 2
+    float* sEcs = small + SM_EC;   // [4][64], slot c % 4
+    float* sGC = small + SM_GC;    // [4], slot c % 4
+    float* sGB = small + SM_GB;    // [2][2][64]: log-decay, beta of chunk c in slot c % 2
     volatile int* abort_flag = &bars->abort;
 
     const int tid = threadIdx.x;
@@ -289,7 +296,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) mbar_init(&bars->dfree[b], kChain);
         mbar_init(&bars->gram, 1);
-        mbar_init(&bars->prep_mma, 1);
+        for (int b = 0; b < 2; ++b) mbar_init(&bars->prep_mma[b], 1);
         mbar_init(&bars->c1, 1);
         mbar_init(&bars->c2, 1);
         mbar_init(&bars->c3, 1);
@@ -315,9 +322,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
         float* M = reinterpret_cast<float*>(sm + OFF_AT);
         uint8_t* t12 = sm + OFF_T12;
-        uint32_t prep_phase = 0;
-        bool mma_pending = false;
-        int gram_issued = -1, gram_waited = -1;
+        int gram_issued = -1, gram_waited = -1, uw_issued = -1;
         // Gram product [Q; K] K^T of chunk cc into R_G (issued by thread 64 once the chunk has landed)
         auto issue_gram = [&](int cc) {
             const uint32_t st_c = sbase + (cc % kStages) * STAGE_BYTES;
@@ -330,65 +335,94 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             mma_commit(&bars->gram);
         };
-        // decays of chunk cc (threads 0..63): G = inclusive cumulative sum inside the chunk
-        auto scan_decays = [&](int cc, float gv, float bv) {
+        // the next chunk's Gram product (R_G has been read) if its inputs have landed;
+        // otherwise it is issued when that chunk starts
+        auto try_gram_next = [&](int c) {
+            if (pt == 64 && gram_issued <= c && c + 1 < n_chunks &&
+                mbar_try_wait(&bars->full[(c + 1) % kStages], ((c + 1) / kStages) & 1)) {
+                issue_gram(c + 1);
+                gram_issued = c + 1;
+            }
+        };
+        // decay inputs of chunk cc into slot cc % 2 by 64 consecutive threads (i = 0..63; zero
+        // past the end).  The copies are asynchronous so that barriers do not wait for them;
+        // the thread that fetched element i is the one that scans it.
+        auto fetch_decays = [&](int cc, int i) {
+            float* dst = sGB + 128 * (cc & 1);
+            const int tn = cc * kC + i;
+            if (tn < S) {
+                cp_async_4(dst + i, g_log + (size_t)bh * S + tn);
+                cp_async_4(dst + 64 + i, beta + (size_t)bh * S + tn);
+            } else {
+                dst[i] = 0.f;
+                dst[64 + i] = 0.f;
+            }
+            cp_async_commit();
+        };
+        // decays of chunk cc (64 consecutive threads): G = inclusive cumulative sum inside the chunk
+        auto scan_decays = [&](int cc, int i) {
+            cp_async_wait_all();
+            const int sl = cc & 1;
+            const float gv = sGB[128 * sl + i], bv = sGB[128 * sl + 64 + i];
+            float* gam = sGam + 64 * sl;
             float x = gv;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const float u = __shfl_up_sync(0xffffffffu, x, o);
                 if (lane >= o) x += u;
             }
-            sGam[pt] = x;  // warp partials
+            gam[i] = x;  // warp partials
             named_bar_sync(BAR_SCAN, 64);
-            const float G = x + (pt >= 32 ? sGam[31] : 0.f);
-            const float GC = sGam[63] + sGam[31];
+            const float G = x + (i >= 32 ? gam[31] : 0.f);
+            const float GC = gam[63] + gam[31];
             named_bar_sync(BAR_SCAN, 64);
-            sG[pt] = G * kLog2e;
-            sGam[pt] = exp2_approx(G * kLog2e);
-            sBet[pt] = bv;
-            sEcs[64 * (cc & 3) + pt] = exp2_approx((GC - G) * kLog2e);
-            if (pt == 0) sGC[cc & 3] = exp2_approx(GC * kLog2e);
+            sG[64 * sl + i] = G * kLog2e;
+            gam[i] = exp2_approx(G * kLog2e);
+            sBet[64 * sl + i] = bv;
+            sEcs[64 * (cc & 3) + i] = exp2_approx((GC - G) * kLog2e);
+            if (i == 0) sGC[cc & 3] = exp2_approx(GC * kLog2e);
         };
-        // decay inputs: chunk 0 now, chunk 1 prefetched (threads 0..63)
-        float g_next = 0.f, b_next = 0.f;
+        // chunk 0's decays now (threads 0..63); chunk 1's inputs fetched by the threads that
+        // scan it (128..191, during the first chunk's diagonal solve)
         if (pt < 64) {
-            const float g0 = (pt < S) ? g_log[(size_t)bh * S + pt] : 0.f;
-            const float b0 = (pt < S) ? beta[(size_t)bh * S + pt] : 0.f;
-            g_next = (kC + pt < S) ? g_log[(size_t)bh * S + kC + pt] : 0.f;
-            b_next = (kC + pt < S) ? beta[(size_t)bh * S + kC + pt] : 0.f;
-            scan_decays(0, g0, b0);
+            fetch_decays(0, pt);
+            scan_decays(0, pt);
+        } else if (pt >= 128 && pt < 192) {
+            fetch_decays(1, pt - 128);
         }
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c % kStages;  // input stage
-            const int db = c & 1;       // TMEM buffer R_D
+            const int db = c & 1;       // TMEM buffer R_D, U/W barrier slot
             const uint32_t st_s = sbase + s * STAGE_BYTES;
             uint8_t* st = sm + s * STAGE_BYTES;
-            // ---- chunk inputs have landed (the Gram product was issued at the end of the
-            //      previous chunk; every thread still observes the load's completion)
+            const float* cG = sG + 64 * (c & 1);
+            const float* cGam = sGam + 64 * (c & 1);
+            const float* cBet = sBet + 64 * (c & 1);
+            // ---- chunk inputs and its Gram product (normally issued during the previous chunk).
+            //      A failed wait skips this thread's work; the vote below stops every prep thread.
             bool fail = !mbar_wait_or_abort(&bars->full[s], (c / kStages) & 1, abort_flag);
             if (!fail && pt == 64 && gram_issued < c) {
                 issue_gram(c);
                 gram_issued = c;
             }
             if (!fail) fail = !mbar_wait_or_abort(&bars->gram, c & 1, abort_flag);
-            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
-            gram_waited = c;
+            if (!fail) gram_waited = c;
             tc_fence_after();
 
             // ---- P (bf16, lanes 0..63) and A (fp32, lanes 64..127); 32 columns per thread
-            {
+            if (!fail) {
                 const bool is_a = L >= 64;
                 const int r = is_a ? L - 64 : L;
                 const int j0 = hh * 32;
                 float x[32];
                 tmem_ld32(trow + COL_G + j0, x);
-                const float Gr = sG[r];
-                const float br = is_a ? sBet[r] : 1.f;
+                const float Gr = cG[r];
+                const float br = is_a ? cBet[r] : 1.f;
                 const int lim = is_a ? r : r + 1;  // A: j < r, P: j <= r
                 tmem_wait_ld();
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const float4 gj = *reinterpret_cast<const float4*>(sG + j0 + 4 * q);
+                    const float4 gj = *reinterpret_cast<const float4*>(cG + j0 + 4 * q);
                     const float gv[4] = {gj.x, gj.y, gj.z, gj.w};
 #pragma unroll
                     for (int u = 0; u < 4; ++u) {
@@ -407,16 +441,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                     st_row_bf16x32(st + ST_P, r, j0 * 2, x);
                 }
             }
-            named_bar_sync(BAR_PREP, kPrep);
+            tc_fence_before();  // R_G read before the next Gram product
+            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
+            try_gram_next(c);
 
-            // ---- warps 0..3: diagonal blocks of T;  warps 4..7: Q' = diag(gamma) Q in place
+            // ---- warps 0..3: diagonal blocks of T;  warps 4..7: Q' = diag(gamma) Q in place, and
+            //      warps 4, 5 the next chunk's decays (another slot) and the inputs of the one after
             if (warp < 4) {
                 solve_diag_block(M, warp, lane);
             } else {
                 const int qt = pt - 128;  // 0..127: row qt / 2 of the Q box qt % 2
-                scale_row_chunks<8>(st + ((qt & 1) ? ST_Q1 : ST_Q0), qt >> 1, 0, sGam[qt >> 1]);
+                scale_row_chunks<8>(st + ((qt & 1) ? ST_Q1 : ST_Q0), qt >> 1, 0, cGam[qt >> 1]);
+                if (warp < 6) {
+                    if (c + 1 < n_chunks) scan_decays(c + 1, qt);
+                    fetch_decays(c + 2, qt);
+                }
             }
-            named_bar_sync(BAR_PREP, kPrep);
+            // chunk c - 1's U/W product has read T diag(beta), T diag(beta gamma): wait before
+            // the levels below rewrite them
+            if (c >= 1) fail = !mbar_wait_or_abort(&bars->prep_mma[(c - 1) & 1], ((c - 1) >> 1) & 1, abort_flag);
+            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
             if (warp < 4) {
                 // ---- level 1 (warps 0..3): T_10 = -T_11 A_10 T_00,  T_32 = -T_33 A_32 T_22
                 const int blk = warp >> 1, nt = warp & 1;
@@ -442,7 +486,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_tf32_16x8x8(y, a, bf);
                 }
                 store_cfrag(M, AT_STRIDE, rb, cb + 8 * nt, g, t, y, -1.f);
-                store_t12_frag(t12, sBet, sGam, rb, cb + 8 * nt, g, t, y, -1.f);
+                store_t12_frag(t12, cBet, cGam, rb, cb + 8 * nt, g, t, y, -1.f);
             } else {
                 // ---- warps 4..7 meanwhile: the diagonal blocks and the zero upper blocks of
                 //      T diag(beta), T diag(beta gamma); row qt / 2, 16-byte chunks 4 (qt % 2) ..
@@ -461,8 +505,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                         float a1[8], a2[8];
 #pragma unroll
                         for (int u = 0; u < 8; ++u) {
-                            a1[u] = tv[u] * sBet[8 * q + u];
-                            a2[u] = a1[u] * sGam[8 * q + u];
+                            a1[u] = tv[u] * cBet[8 * q + u];
+                            a2[u] = a1[u] * cGam[8 * q + u];
                         }
                         w1 = make_uint4(pack_bf16x2(a1[0], a1[1]), pack_bf16x2(a1[2], a1[3]), pack_bf16x2(a1[4], a1[5]),
                                         pack_bf16x2(a1[6], a1[7]));
@@ -499,11 +543,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                     load_bfrag(M, AT_STRIDE, 8 * ks, 32 + 8 * nt, g, t, bf);
                     mma_tf32_16x8x8(y, a, bf);
                 }
-                store_t12_frag(t12, sBet, sGam, 32 + 16 * mt, 8 * nt, g, t, y, -1.f);
+                store_t12_frag(t12, cBet, cGam, 32 + 16 * mt, 8 * nt, g, t, y, -1.f);
             }
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_PREP, kPrep);
+            // ---- chunk c goes to the chain (P, Q' written; its U/W product completes on
+            //      prep_mma[c % 2], which the chain waits for itself)
+            mbar_arrive(&bars->ready[s]);
             // ---- [U^T | W^T] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T] into R_D[db],
             //      once the chain has read chunk c - 2's output from that buffer
             if (pt == 64) {
@@ -518,53 +565,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int kk = 0; kk < 4; ++kk)
                         mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
                                  make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
-                    mma_commit(&bars->prep_mma);
+                    mma_commit(&bars->prep_mma[db]);
+                    uw_issued = c;
                 }
-                // the next chunk's Gram product now if its inputs have already landed (R_G
-                // has been read); otherwise it is issued when the next chunk starts
-                if (free_ok && c + 1 < n_chunks &&
-                    mbar_try_wait(&bars->full[(c + 1) % kStages], ((c + 1) / kStages) & 1)) {
-                    issue_gram(c + 1);
-                    gram_issued = c + 1;
-                }
+                try_gram_next(c);
             }
-            // the next chunk's decays (nobody reads this chunk's G, gamma, beta any more)
-            if (pt < 64 && c + 1 < n_chunks) {
-                scan_decays(c + 1, g_next, b_next);
-                const int tn = (c + 2) * kC + pt;
-                g_next = (tn < S) ? g_log[(size_t)bh * S + tn] : 0.f;
-                b_next = (tn < S) ? beta[(size_t)bh * S + tn] : 0.f;
-            }
-            mma_pending = true;
-            fail = !mbar_wait_or_abort(&bars->prep_mma, prep_phase, abort_flag);
-            if (named_bar_any(BAR_PREP, kPrep, fail)) break;
-            prep_phase ^= 1;
-            mma_pending = false;
-            tc_fence_after();
-            // ---- -W over V (the U product has read V), K-major: thread (dk = L, tokens
-            //      32 hh ..) writes column L % 64 of box L / 64, rows 32 hh .. 32 hh + 31;
-            //      then the output half of R_D[db] is zeroed for the chain's accumulation
-            {
-                float x[32];
-                const uint32_t waddr = trow + COL_D + 128 * db + 64 + hh * 32;
-                tmem_ld32(waddr, x);
-                tmem_wait_ld();
-                uint8_t* box = st + ((L >> 6) ? ST_VW1 : ST_VW0);
-                const uint32_t cb = 2u * (uint32_t)(L & 63);
-#pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(32 * hh + i, cb)) = __float2bfloat16_rn(-x[i]);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) x[i] = 0.f;
-                tmem_st32(waddr, x);
-                tmem_wait_st();
-            }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            mbar_arrive(&bars->ready[s]);
         }
+        if (pt >= 128 && pt < 192) cp_async_wait_all();
         if (pt == 64) {  // drain what this thread issued (a completed phase returns at once)
-            if (mma_pending) (void)mbar_wait(&bars->prep_mma, prep_phase);
+            if (uw_issued >= 0) (void)mbar_wait(&bars->prep_mma[uw_issued & 1], (uw_issued >> 1) & 1);
             if (gram_issued > gram_waited) (void)mbar_wait(&bars->gram, gram_issued & 1);
         }
     } else {
@@ -614,12 +623,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int db = c & 1;       // TMEM buffer R_D
             const uint32_t st_s = sbase + s * STAGE_BYTES;
             uint8_t* st = sm + s * STAGE_BYTES;
+            // ---- chunk c from prep, and its U/W product
             bool fail = !mbar_wait_or_abort(&bars->ready[s], (c / kStages) & 1, abort_flag);
-            if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
-            const float gC = sGC[c & 3];
-            const float ec_row = sEcs[64 * (c & 3) + (ct >> 1)];
+            if (!fail) fail = !mbar_wait_or_abort(&bars->prep_mma[db], (c >> 1) & 1, abort_flag);
             tc_fence_after();
+            if (!fail) {
+                // -W over V (the U product has read V), K-major: thread (dk = ct) writes column
+                // ct % 64 of box ct / 64, rows 0..63; then the output half of R_D[db] is zeroed
+                // for the accumulation below
+                float x[64];
+                const uint32_t waddr = trow + COL_D + 128 * db + 64;
+                tmem_ld32(waddr, *reinterpret_cast<float(*)[32]>(x));
+                tmem_ld32(waddr + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                tmem_wait_ld();
+                uint8_t* box = st + ((ct >> 6) ? ST_VW1 : ST_VW0);
+                const uint32_t cb = 2u * (uint32_t)(ct & 63);
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(i, cb)) = __float2bfloat16_rn(-x[i]);
+#pragma unroll
+                for (int i = 0; i < 64; ++i) x[i] = 0.f;
+                tmem_st32(waddr, *reinterpret_cast<const float(*)[32]>(x));
+                tmem_st32(waddr + 32, *reinterpret_cast<const float(*)[32]>(x + 32));
+                tmem_wait_st();
+            }
+            fence_proxy_async_smem();
+            tc_fence_before();
+            if (ct == 0) tma_store_wait_read0();  // the out tile of chunk c - 2 has been read
+            if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             if (ct == 0) {
+                tc_fence_after();
                 // [Delta^T | O^T] += S0^T [-W; Q']^T: Delta^T = U^T - S0^T W^T, O^T = S0^T Q'^T
                 // (A = the bf16 state in TMEM, 8 columns per 16-wide K step)
 #pragma unroll
@@ -630,43 +663,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bars->c1);
             }
             issued1 = c;
-            // K~ = diag(exp(G_C - G)) K in place while the products run (prep's W product has
-            // read K; the state increment below reads K~): row ct / 2 of box ct % 2
-            scale_row_chunks<8>(st + ((ct & 1) ? ST_K1 : ST_K0), ct >> 1, 0, ec_row);
-            // S^T <- gamma_C S^T in TMEM while the products run; the increment accumulates onto it
+            if (c == 0) {
+                // S^T <- gamma_C S^T for the first chunk (later chunks get it with the bf16 copy)
+                const float gC = sGC[0];
 #pragma unroll 1
-            for (int c0 = 0; c0 < kD; c0 += 32) {
-                float x[32];
-                tmem_ld32(trow + COL_S + c0, x);
-                tmem_wait_ld();
+                for (int c0 = 0; c0 < kD; c0 += 32) {
+                    float x[32];
+                    tmem_ld32(trow + COL_S + c0, x);
+                    tmem_wait_ld();
 #pragma unroll
-                for (int j = 0; j < 32; ++j) x[j] *= gC;
-                tmem_st32(trow + COL_S + c0, x);
+                    for (int j = 0; j < 32; ++j) x[j] *= gC;
+                    tmem_st32(trow + COL_S + c0, x);
+                }
+                tmem_wait_st();
+            } else {
+                // output of the previous chunk (its accumulator completed before the barrier that
+                // ended the previous iteration) while the product runs; prep may then reuse the buffer
+                tc_fence_after();
+                write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * ((c - 1) & 1) + 64, ct, scale);
+                tc_fence_before();
+                mbar_arrive(&bars->dfree[(c - 1) & 1]);
+                fence_proxy_async_smem();
             }
-            tmem_wait_st();
             fail = !mbar_wait_or_abort(&bars->c1, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             tc_fence_after();
-            // Delta^T as a K-major bf16 operand over -W and Q' (both consumed by the product above)
+            // Delta^T as a K-major bf16 operand over [-W; Q'] (dk 0..63), and Delta^T diag(exp(G_C - G))
+            // over [-W; Q'] (dk 64..127), both consumed by the product above
             {
-                float x[32];
-                tmem_ld32(trow + COL_D + 128 * db, x);
-                tmem_wait_ld();
-                st_row_bf16x32(st + ST_DT, ct, 0, x);
-                tmem_ld32(trow + COL_D + 128 * db + 32, x);
-                tmem_wait_ld();
-                st_row_bf16x32(st + ST_DT, ct, 64, x);
+                const float* ec = sEcs + 64 * (c & 3);
+#pragma unroll 1
+                for (int h = 0; h < 2; ++h) {
+                    float x[32];
+                    tmem_ld32(trow + COL_D + 128 * db + 32 * h, x);
+                    tmem_wait_ld();
+                    st_row_bf16x32(st + ST_DT, ct, 64 * h, x);
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) {
+                        const float4 e = *reinterpret_cast<const float4*>(ec + 32 * h + 4 * q);
+                        x[4 * q] *= e.x;
+                        x[4 * q + 1] *= e.y;
+                        x[4 * q + 2] *= e.z;
+                        x[4 * q + 3] *= e.w;
+                    }
+                    st_row_bf16x32(st + ST_DT2, ct, 64 * h, x);
+                }
             }
             fence_proxy_async_smem();
             tc_fence_before();
-            if (ct == 0) tma_store_wait_read0();  // the out tile of chunk c-2 has been read
             named_bar_sync(BAR_CHAIN, kChain);
             if (ct == 0) {
                 tc_fence_after();
-                // S^T += Delta^T K~
+                // S^T += (Delta^T diag(exp(G_C - G))) K
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_S, make_sdesc(st_s + ST_DT + kk * 32, 16, 1024),
+                    mma_bf16(tmem + COL_S, make_sdesc(st_s + ST_DT2 + kk * 32, 16, 1024),
                              make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024), IDESC_N128_KM, 1);
                 mma_commit(&bars->c2);
                 // O^T += Delta^T P^T
@@ -675,15 +726,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_DT + kk * 32, 16, 1024),
                              make_sdesc(st_s + ST_P + kk * 32, 16, 1024), IDESC_N64_KK, 1);
                 mma_commit(&bars->c3);
+                if (c >= 1) {  // out tile of chunk c - 1
+                    tma_store_3d(&tm_o, sm + OFF_OUT, 0, (c - 1) * kC, bh);
+                    tma_store_commit();
+                }
             }
             issued23 = c;
-            // output of the previous chunk (its accumulator completed last iteration); prep may
-            // then reuse that buffer
-            if (c >= 1) {
-                write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * ((c - 1) & 1) + 64, ct, scale);
-                tc_fence_before();
-                mbar_arrive(&bars->dfree[(c - 1) & 1]);
-            }
             fail = !mbar_wait_or_abort(&bars->c2, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             tc_fence_after();
@@ -697,23 +745,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (c + kStages + 1 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, c + kStages + 1, bhk, bh);
                 }
             }
-            // bf16 copy of the new state for the next chunk's first product
+            // bf16 copy of the new state for the next chunk's first product, and the state
+            // scaled by the next chunk's gamma_C, onto which its increment accumulates
+            {
+                const bool more = c + 1 < n_chunks;
+                const float gN = more ? sGC[(c + 1) & 3] : 1.f;
 #pragma unroll 1
-            for (int h64 = 0; h64 < 2; ++h64) {
-                float x[64];
-                tmem_ld32(trow + COL_S + 64 * h64, *reinterpret_cast<float(*)[32]>(x));
-                tmem_ld32(trow + COL_S + 64 * h64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                tmem_wait_ld();
-                store_state_bf16(h64, x);
+                for (int h64 = 0; h64 < 2; ++h64) {
+                    float x[64];
+                    tmem_ld32(trow + COL_S + 64 * h64, *reinterpret_cast<float(*)[32]>(x));
+                    tmem_ld32(trow + COL_S + 64 * h64 + 32, *reinterpret_cast<float(*)[32]>(x + 32));
+                    tmem_wait_ld();
+                    store_state_bf16(h64, x);
+                    if (more) {
+#pragma unroll
+                        for (int j = 0; j < 64; ++j) x[j] *= gN;
+                        tmem_st32(trow + COL_S + 64 * h64, *reinterpret_cast<const float(*)[32]>(x));
+                        tmem_st32(trow + COL_S + 64 * h64 + 32, *reinterpret_cast<const float(*)[32]>(x + 32));
+                    }
+                }
             }
             tmem_wait_st();
-            fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_CHAIN, kChain);
-            if (ct == 0 && c >= 1) {  // out tile of chunk c - 1
-                tma_store_3d(&tm_o, sm + OFF_OUT, 0, (c - 1) * kC, bh);
-                tma_store_commit();
-            }
         }
         ok = !named_bar_any(BAR_CHAIN, kChain, !ok || *abort_flag != 0);
         if (ok && n_chunks > 0) {

@@ -143,6 +143,14 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c
                  "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// 4-byte asynchronous copy global -> shared.  It is not tracked by the register
+// scoreboard, so barriers and mbarrier waits do not stall on it; the issuing
+// thread sees the data after cp_async_wait_all.
+__device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 // 3-D tiled store shared -> global (rows outside the tensor are clipped).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
     asm volatile(
