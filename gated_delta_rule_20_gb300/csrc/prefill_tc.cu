@@ -99,7 +99,7 @@ constexpr uint32_t LOAD_BYTES = 49152;
 constexpr uint32_t OFF_T12 = kStages * STAGE_BYTES;  // T diag(beta), T diag(beta gamma): [64 r][64 j] bf16 each
 constexpr uint32_t OFF_AT = OFF_T12 + 16384;   // fp32 A, solved in place into T: [64][68]; its upper-right
 constexpr int AT_STRIDE = 68;                  // 32 x 32 quadrant (never read as T) is the solve's scratch
-constexpr uint32_t OFF_OUT = OFF_AT + 17408;   // out tile [64 r][128 dv] bf16, unswizzled
+constexpr uint32_t OFF_OUT = OFF_AT + 17408;   // out tile: two [64 r][64 dv] bf16 boxes (dv halves), 128-byte swizzle
 constexpr uint32_t OFF_SMALL = OFF_OUT + 16384;
 // small area (floats), per chunk c in slot c % 2:  G2[2][64] = log2(e) x cumulative
 // log-decay, gam[2][64] = exp(G), bet[2][64];  in slot c % 4 (read by the chain up to three
@@ -154,18 +154,31 @@ __device__ __forceinline__ void scale_row_chunks(uint8_t* tile, int row, int q0,
     }
 }
 
-// Output: thread ct holds column dv = ct of O^T / scale in TMEM (64 tokens);
-// write scale * O into the unswizzled [64 tokens][128 dv] bf16 staging tile.
-__device__ __forceinline__ void write_out_tile(uint8_t* tile, uint32_t taddr, int ct, float scale) {
-    float x0[32], x1[32];
-    tmem_ld32(taddr, x0);
-    tmem_ld32(taddr + 32, x1);
-    tmem_wait_ld();
-    __nv_bfloat16* ob = reinterpret_cast<__nv_bfloat16*>(tile) + ct;
+// Transposing store of one warp's 32 TMEM lanes x 64 fp32 columns, times `mul`, as bf16
+// into a pair of K-major [64 rows][64] boxes with the 128-byte swizzle (`box_stride` bytes
+// apart): lane l0 + i, column j goes to row j, element (l0 + i) % 64 of box (l0 + i) / 64.
+// `taddr` addresses lane l0 = 32 (warp % 4) and the first column.  Each 16-lane half is
+// read as m16n8 accumulator fragments and written with stmatrix.trans, 16 bytes per row.
+__device__ __forceinline__ void tmem_store_transposed(uint32_t taddr, uint8_t* box0, uint32_t box_stride, int l0,
+                                                      float mul, int lane) {
+    const int mi = lane >> 3, rr = lane & 7;  // this thread addresses row rr of matrix mi
 #pragma unroll
-    for (int r = 0; r < 32; ++r) {
-        ob[r * kD] = __float2bfloat16_rn(scale * x0[r]);
-        ob[(r + 32) * kD] = __float2bfloat16_rn(scale * x1[r]);
+    for (int hl = 0; hl < 2; ++hl) {
+        float r[32];
+        tmem_ld16x256_x8(taddr + ((uint32_t)(16 * hl) << 16), r);
+        tmem_wait_ld();
+        uint32_t p[16];  // p[2k]: lanes +0..7, p[2k + 1]: lanes +8..15, columns 8k .. 8k + 7
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            p[2 * k] = pack_bf16x2(r[4 * k] * mul, r[4 * k + 1] * mul);
+            p[2 * k + 1] = pack_bf16x2(r[4 * k + 2] * mul, r[4 * k + 3] * mul);
+        }
+        const int dl = l0 + 16 * hl + 8 * (mi & 1);  // first lane of the matrix this thread addresses
+        const uint32_t box = smem_u32(box0 + (dl >> 6) * box_stride);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2)
+            stmatrix_x4_trans(box + sw128_offset(8 * (k + (mi >> 1)) + rr, 2 * (dl & 63)), p[2 * k], p[2 * k + 1],
+                              p[2 * k + 2], p[2 * k + 3]);
     }
 }
 
@@ -628,23 +641,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (!fail) fail = !mbar_wait_or_abort(&bars->prep_mma[db], (c >> 1) & 1, abort_flag);
             tc_fence_after();
             if (!fail) {
-                // -W over V (the U product has read V), K-major: thread (dk = ct) writes column
-                // ct % 64 of box ct / 64, rows 0..63; then the output half of R_D[db] is zeroed
-                // for the accumulation below
-                float x[64];
+                // -W over V (the U product has read V), K-major: dk on the rows' elements, tokens
+                // on the rows; then the output half of R_D[db] is zeroed for the accumulation below
                 const uint32_t waddr = trow + COL_D + 128 * db + 64;
-                tmem_ld32(waddr, *reinterpret_cast<float(*)[32]>(x));
-                tmem_ld32(waddr + 32, *reinterpret_cast<float(*)[32]>(x + 32));
-                tmem_wait_ld();
-                uint8_t* box = st + ((ct >> 6) ? ST_VW1 : ST_VW0);
-                const uint32_t cb = 2u * (uint32_t)(ct & 63);
+                tmem_store_transposed(waddr, st + ST_VW0, ST_HALF, (warp & 3) * 32, -1.f, lane);
+                float z[32];
 #pragma unroll
-                for (int i = 0; i < 64; ++i)
-                    *reinterpret_cast<__nv_bfloat16*>(box + sw128_offset(i, cb)) = __float2bfloat16_rn(-x[i]);
-#pragma unroll
-                for (int i = 0; i < 64; ++i) x[i] = 0.f;
-                tmem_st32(waddr, *reinterpret_cast<const float(*)[32]>(x));
-                tmem_st32(waddr + 32, *reinterpret_cast<const float(*)[32]>(x + 32));
+                for (int i = 0; i < 32; ++i) z[i] = 0.f;
+                tmem_st32(waddr, z);
+                tmem_st32(waddr + 32, z);
                 tmem_wait_st();
             }
             fence_proxy_async_smem();
@@ -680,7 +685,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // output of the previous chunk (its accumulator completed before the barrier that
                 // ended the previous iteration) while the product runs; prep may then reuse the buffer
                 tc_fence_after();
-                write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * ((c - 1) & 1) + 64, ct, scale);
+                tmem_store_transposed(trow + COL_D + 128 * ((c - 1) & 1) + 64, sm + OFF_OUT, 8192, (warp & 3) * 32,
+                                      scale, lane);
                 tc_fence_before();
                 mbar_arrive(&bars->dfree[(c - 1) & 1]);
                 fence_proxy_async_smem();
@@ -692,21 +698,22 @@ __global__ void __launch_bounds__(kThreads, 1)
             // over [-W; Q'] (dk 64..127), both consumed by the product above
             {
                 const float* ec = sEcs + 64 * (c & 3);
-#pragma unroll 1
+                float x[2][32];
+                tmem_ld32(trow + COL_D + 128 * db, x[0]);
+                tmem_ld32(trow + COL_D + 128 * db + 32, x[1]);
+                tmem_wait_ld();
+#pragma unroll
                 for (int h = 0; h < 2; ++h) {
-                    float x[32];
-                    tmem_ld32(trow + COL_D + 128 * db + 32 * h, x);
-                    tmem_wait_ld();
-                    st_row_bf16x32(st + ST_DT, ct, 64 * h, x);
+                    st_row_bf16x32(st + ST_DT, ct, 64 * h, x[h]);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 e = *reinterpret_cast<const float4*>(ec + 32 * h + 4 * q);
-                        x[4 * q] *= e.x;
-                        x[4 * q + 1] *= e.y;
-                        x[4 * q + 2] *= e.z;
-                        x[4 * q + 3] *= e.w;
+                        x[h][4 * q] *= e.x;
+                        x[h][4 * q + 1] *= e.y;
+                        x[h][4 * q + 2] *= e.z;
+                        x[h][4 * q + 3] *= e.w;
                     }
-                    st_row_bf16x32(st + ST_DT2, ct, 64 * h, x);
+                    st_row_bf16x32(st + ST_DT2, ct, 64 * h, x[h]);
                 }
             }
             fence_proxy_async_smem();
@@ -728,6 +735,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mma_commit(&bars->c3);
                 if (c >= 1) {  // out tile of chunk c - 1
                     tma_store_3d(&tm_o, sm + OFF_OUT, 0, (c - 1) * kC, bh);
+                    tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, (c - 1) * kC, bh);
                     tma_store_commit();
                 }
             }
@@ -779,11 +787,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             named_bar_sync(BAR_CHAIN, kChain);
             tc_fence_after();
-            write_out_tile(sm + OFF_OUT, trow + COL_D + 128 * (c & 1) + 64, ct, scale);
+            tmem_store_transposed(trow + COL_D + 128 * (c & 1) + 64, sm + OFF_OUT, 8192, (warp & 3) * 32, scale, lane);
             fence_proxy_async_smem();
             named_bar_sync(BAR_CHAIN, kChain);
             if (ct == 0) {
                 tma_store_3d(&tm_o, sm + OFF_OUT, 0, c * kC, bh);
+                tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, c * kC, bh);
                 tma_store_commit();
             }
             float* Sg = state + (size_t)bh * kD * kD;
@@ -857,7 +866,7 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     CUtensorMap tq, tk, tv, to;
     if (!encode_bf16_3d(&tq, p.q, p.B * p.Hk, p.S, 64, true) || !encode_bf16_3d(&tk, p.k, p.B * p.Hk, p.S, 64, true) ||
         !encode_bf16_3d(&tv, p.v, p.B * p.Hv, p.S, 64, true) ||
-        !encode_bf16_3d(&to, p.out, p.B * p.Hv, p.S, 128, false))
+        !encode_bf16_3d(&to, p.out, p.B * p.Hv, p.S, 64, true))
         return GDN_ERR_CUDA;
     // the shared-memory opt-in is set once per device
     static std::mutex mu;

@@ -143,6 +143,14 @@ __device__ __forceinline__ void tma_prefetch_l2_3d(const CUtensorMap* map, int c
                  "r"(c0), "r"(c1), "r"(c2)
                  : "memory");
 }
+// Four 8x8 b16 matrices stored transposed: register m of thread t holds row t/4,
+// columns 2(t%4), 2(t%4)+1 of matrix m (low half first); thread i gives the address of
+// row i % 8 of the stored (transposed) matrix i / 8, 16 contiguous bytes.
+__device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t m0, uint32_t m1, uint32_t m2, uint32_t m3) {
+    asm volatile("stmatrix.sync.aligned.m8n8.x4.trans.shared.b16 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(m0), "r"(m1),
+                 "r"(m2), "r"(m3)
+                 : "memory");
+}
 // 4-byte asynchronous copy global -> shared.  It is not tracked by the register
 // scoreboard, so barriers and mbarrier waits do not stall on it; the issuing
 // thread sees the data after cp_async_wait_all.
@@ -195,6 +203,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&r)[32]) {
           "=f"(r[15]), "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]),
           "=f"(r[22]), "=f"(r[23]), "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]),
           "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
+        : "r"(taddr));
+}
+// 16 lanes starting at the address's lane, 64 columns (.16x256b, 8 repeats): for
+// k = 0..7, thread t gets r[4k], r[4k+1] = lane t/4, columns 8k + 2(t%4) and + 1, and
+// r[4k+2], r[4k+3] = the same columns of lane t/4 + 8 (the m16n8 accumulator layout).
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t taddr, float (&r)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+        : "=f"(r[0]), "=f"(r[1]), "=f"(r[2]), "=f"(r[3]), "=f"(r[4]), "=f"(r[5]), "=f"(r[6]), "=f"(r[7]),
+          "=f"(r[8]), "=f"(r[9]), "=f"(r[10]), "=f"(r[11]), "=f"(r[12]), "=f"(r[13]), "=f"(r[14]), "=f"(r[15]),
+          "=f"(r[16]), "=f"(r[17]), "=f"(r[18]), "=f"(r[19]), "=f"(r[20]), "=f"(r[21]), "=f"(r[22]), "=f"(r[23]),
+          "=f"(r[24]), "=f"(r[25]), "=f"(r[26]), "=f"(r[27]), "=f"(r[28]), "=f"(r[29]), "=f"(r[30]), "=f"(r[31])
         : "r"(taddr));
 }
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&r)[32]) {
