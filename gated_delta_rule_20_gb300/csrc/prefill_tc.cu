@@ -67,14 +67,16 @@ constexpr int kC = 64;   // tokens per chunk
 constexpr int kD = 128;  // Dk = Dv
 constexpr int kPrep = 256;
 constexpr int kChain = 128;
-constexpr int kThreads = kPrep + kChain;
+constexpr int kHelp = 128;
+constexpr int kThreads = kPrep + kChain + kHelp;
 constexpr uint32_t kTmemCols = 512;
 
 // TMEM columns (32-bit, 128 lanes each)
 constexpr uint32_t COL_G = 0;     // 64: Gram
-constexpr uint32_t COL_D = 64;    // 2 x 128, chunk c in buffer c % 2: [U^T -> Delta^T | W^T, then output]
+constexpr uint32_t COL_D = 64;    // 2 x 128, chunk c in buffer c % 2: [U^T -> Delta^T -> bf16 Delta^T | W^T, then output]
 constexpr uint32_t COL_S = 320;   // 128: the fp32 state S^T (lane dv, column dk)
-constexpr uint32_t COL_SA = 448;  // 64: the state as bf16 pairs, the A operand of the chunk's first product
+constexpr uint32_t COL_SA = 448;  // 64: the state as bf16 pairs, the A operand of the chunk's first product;
+                                  // between that product and the state's next copy, bf16 Delta^T diag(exp(G_C - G))
 
 // Shared memory (bytes from a 1024-aligned base).  bf16 tiles: rows of 128 B
 // with the 128-byte swizzle.
@@ -91,10 +93,6 @@ constexpr uint32_t ST_VW1 = ST_VW0 + ST_HALF;
 constexpr uint32_t ST_Q1 = ST_Q0 + ST_HALF;
 constexpr uint32_t ST_K1 = ST_K0 + ST_HALF;
 constexpr uint32_t ST_P = 49152;     // P [64 r][64 j]
-// Delta^T [128 dv][64 j] K-major bf16, and Delta^T diag(exp(G_C - G)) likewise: written over
-// [-W; Q'] (dk 0..63 and dk 64..127) once the chain's first product has read them
-constexpr uint32_t ST_DT = 0;
-constexpr uint32_t ST_DT2 = ST_HALF;
 constexpr uint32_t LOAD_BYTES = 49152;
 constexpr uint32_t OFF_T12 = kStages * STAGE_BYTES;  // T diag(beta), T diag(beta gamma): [64 r][64 j] bf16 each
 constexpr uint32_t OFF_AT = OFF_T12 + 16384;   // fp32 A, solved in place into T: [64][68]; its upper-right
@@ -121,6 +119,7 @@ constexpr uint32_t BAR_PREP = 1;   // named barrier: the 8 prep warps
 constexpr uint32_t BAR_CHAIN = 2;  // named barrier: the 4 chain warps
 constexpr uint32_t BAR_SCAN = 3;   // prep warps 0, 1 (the decay scan)
 constexpr uint32_t BAR_L1 = 4;     // prep warps 0..3 (level 1 of the solve)
+constexpr uint32_t BAR_HELP = 5;   // the 4 helper warps
 
 // bf16 row writer: 32 fp32 values -> bytes [byte0, byte0 + 64) of a swizzled row.
 __device__ __forceinline__ void st_row_bf16x32(uint8_t* tile, int row, int byte0, const float* x, float mul = 1.f) {
@@ -135,16 +134,16 @@ __device__ __forceinline__ void st_row_bf16x32(uint8_t* tile, int row, int byte0
     }
 }
 
-// Scale `n` 16-byte chunks (8 bf16 each) of one 128-byte row by s, in place,
-// starting at chunk `q0`; the visiting order is rotated by the row so threads
-// on neighbouring rows hit different banks.
-template <int N>
-__device__ __forceinline__ void scale_row_chunks(uint8_t* tile, int row, int q0, float s) {
+// Scale the 8 16-byte chunks (8 bf16 each) of one 128-byte-swizzled row by s, in
+// place.  The chunks are visited in the order of their physical position rotated by
+// the row, so that the 8 threads of a 16-byte access phase, on 8 consecutive rows,
+// touch 8 different bank groups.
+__device__ __forceinline__ void scale_row_sw128(uint8_t* tile, int row, float s) {
     const Bf16Scale sc = make_bf16_scale(s);
-    uint4* p = reinterpret_cast<uint4*>(tile + row * 128);
+    uint4* p = reinterpret_cast<uint4*>(tile + row * 128);  // physical chunks of the row
 #pragma unroll
-    for (int i = 0; i < N; ++i) {
-        const int q = q0 + ((i + row) & (N - 1));
+    for (int i = 0; i < 8; ++i) {
+        const int q = (i + row) & 7;
         uint4 w = p[q];
         w.x = scale_bf16x2(w.x, sc);
         w.y = scale_bf16x2(w.y, sc);
@@ -185,7 +184,10 @@ __device__ __forceinline__ void tmem_store_transposed(uint32_t taddr, uint8_t* b
 struct Bars {
     uint64_t full[kStages];   // TMA -> prep
     uint64_t ready[kStages];  // prep -> chain (kPrep arrivals)
-    uint64_t dfree[2];        // chain has read buffer R_D[b]'s output -> prep may reuse it (kChain arrivals)
+    uint64_t dfree[2];        // helpers have read buffer R_D[b]'s output -> prep may reuse it (kHelp arrivals)
+    uint64_t w_ready;         // helpers -> chain: chunk c's -W written, output half zeroed (kHelp arrivals)
+    uint64_t dt_ready;        // chain -> helpers: chunk c's Delta^T operands written
+    uint64_t req_l2;          // prep -> chain: chunk c's T diag(beta), T diag(beta gamma) written
     uint64_t gram;      // prep: Gram product of a chunk done
     uint64_t prep_mma[2];  // U, W products of chunk c done, slot c % 2 (waited by the chain and by prep)
     uint64_t c1;        // chain: Delta product done
@@ -196,16 +198,19 @@ struct Bars {
 };
 
 // ---------------------------------------------------------------- solve
-// Warp-level tf32 fragments (m16n8k8) of fp32 matrices in shared memory.
+// Warp-level tf32 fragments (m16n8k8) of fp32 matrices in shared memory.  The
+// fp32 bit patterns are passed as they are: the tf32 multiply reads the upper 19
+// bits (sign, exponent, 10 mantissa bits), i.e. the operand truncated to tf32,
+// which saves a conversion per element on the shared conversion pipe.
 __device__ __forceinline__ void load_afrag(const float* M, int ld, int r0, int k0, int g, int t, uint32_t (&a)[4]) {
-    a[0] = f32_to_tf32(M[(r0 + g) * ld + k0 + t]);
-    a[1] = f32_to_tf32(M[(r0 + g + 8) * ld + k0 + t]);
-    a[2] = f32_to_tf32(M[(r0 + g) * ld + k0 + t + 4]);
-    a[3] = f32_to_tf32(M[(r0 + g + 8) * ld + k0 + t + 4]);
+    a[0] = __float_as_uint(M[(r0 + g) * ld + k0 + t]);
+    a[1] = __float_as_uint(M[(r0 + g + 8) * ld + k0 + t]);
+    a[2] = __float_as_uint(M[(r0 + g) * ld + k0 + t + 4]);
+    a[3] = __float_as_uint(M[(r0 + g + 8) * ld + k0 + t + 4]);
 }
 __device__ __forceinline__ void load_bfrag(const float* M, int ld, int k0, int n0, int g, int t, uint32_t (&b)[2]) {
-    b[0] = f32_to_tf32(M[(k0 + t) * ld + n0 + g]);
-    b[1] = f32_to_tf32(M[(k0 + t + 4) * ld + n0 + g]);
+    b[0] = __float_as_uint(M[(k0 + t) * ld + n0 + g]);
+    b[1] = __float_as_uint(M[(k0 + t + 4) * ld + n0 + g]);
 }
 __device__ __forceinline__ void store_cfrag(float* M, int ld, int r0, int n0, int g, int t, const float (&d)[4],
                                             float s) {
@@ -307,7 +312,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->ready[s], kPrep);
         }
-        for (int b = 0; b < 2; ++b) mbar_init(&bars->dfree[b], kChain);
+        for (int b = 0; b < 2; ++b) mbar_init(&bars->dfree[b], kHelp);
+        mbar_init(&bars->w_ready, kHelp);
+        mbar_init(&bars->dt_ready, 1);
+        mbar_init(&bars->req_l2, 1);
         mbar_init(&bars->gram, 1);
         for (int b = 0; b < 2; ++b) mbar_init(&bars->prep_mma[b], 1);
         mbar_init(&bars->c1, 1);
@@ -335,8 +343,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int g = lane >> 2, t = lane & 3;  // mma fragment coordinates
         float* M = reinterpret_cast<float*>(sm + OFF_AT);
         uint8_t* t12 = sm + OFF_T12;
-        int gram_issued = -1, gram_waited = -1, uw_issued = -1;
-        // Gram product [Q; K] K^T of chunk cc into R_G (issued by thread 64 once the chunk has landed)
+        // The Gram products are issued by one thread of warp 7, whose share of the diagonal-solve
+        // step (Q' rows only) is the lightest, so that the issue time hides behind that step.
+        constexpr int kGramThread = 224;
+        int gram_issued = -1, gram_waited = -1;
+        // Gram product [Q; K] K^T of chunk cc into R_G (issued once the chunk has landed)
         auto issue_gram = [&](int cc) {
             const uint32_t st_c = sbase + (cc % kStages) * STAGE_BYTES;
             tc_fence_after();
@@ -351,7 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the next chunk's Gram product (R_G has been read) if its inputs have landed;
         // otherwise it is issued when that chunk starts
         auto try_gram_next = [&](int c) {
-            if (pt == 64 && gram_issued <= c && c + 1 < n_chunks &&
+            if (pt == kGramThread && gram_issued <= c && c + 1 < n_chunks &&
                 mbar_try_wait(&bars->full[(c + 1) % kStages], ((c + 1) / kStages) & 1)) {
                 issue_gram(c + 1);
                 gram_issued = c + 1;
@@ -405,8 +416,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c % kStages;  // input stage
-            const int db = c & 1;       // TMEM buffer R_D, U/W barrier slot
-            const uint32_t st_s = sbase + s * STAGE_BYTES;
             uint8_t* st = sm + s * STAGE_BYTES;
             const float* cG = sG + 64 * (c & 1);
             const float* cGam = sGam + 64 * (c & 1);
@@ -414,7 +423,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // ---- chunk inputs and its Gram product (normally issued during the previous chunk).
             //      A failed wait skips this thread's work; the vote below stops every prep thread.
             bool fail = !mbar_wait_or_abort(&bars->full[s], (c / kStages) & 1, abort_flag);
-            if (!fail && pt == 64 && gram_issued < c) {
+            if (!fail && pt == kGramThread && gram_issued < c) {
                 issue_gram(c);
                 gram_issued = c;
             }
@@ -463,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp < 4) {
                 solve_diag_block(M, warp, lane);
             } else {
-                const int qt = pt - 128;  // 0..127: row qt / 2 of the Q box qt % 2
-                scale_row_chunks<8>(st + ((qt & 1) ? ST_Q1 : ST_Q0), qt >> 1, 0, cGam[qt >> 1]);
+                const int qt = pt - 128;  // 0..127: row qt % 64 of the Q box qt / 64
+                scale_row_sw128(st + ((qt >> 6) ? ST_Q1 : ST_Q0), qt & 63, cGam[qt & 63]);
                 if (warp < 6) {
                     if (c + 1 < n_chunks) scan_decays(c + 1, qt);
                     fetch_decays(c + 2, qt);
@@ -561,52 +570,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_PREP, kPrep);
-            // ---- chunk c goes to the chain (P, Q' written; its U/W product completes on
-            //      prep_mma[c % 2], which the chain waits for itself)
+            // ---- chunk c goes to the chain (P, Q' written; the chain issues its U/W product,
+            //      which completes on prep_mma[c % 2])
             mbar_arrive(&bars->ready[s]);
-            // ---- [U^T | W^T] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T] into R_D[db],
-            //      once the chain has read chunk c - 2's output from that buffer
-            if (pt == 64) {
-                const bool free_ok = (c < 2) || mbar_wait_or_abort(&bars->dfree[db], ((c - 2) >> 1) & 1, abort_flag);
-                tc_fence_after();
-                if (free_ok) {
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + COL_D + 128 * db, make_sdesc(st_s + ST_VW0 + kk * 2048, ST_HALF, 1024),
-                                 make_sdesc(sbase + OFF_T12 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
-                                 make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
-                    mma_commit(&bars->prep_mma[db]);
-                    uw_issued = c;
-                }
-                try_gram_next(c);
-            }
+            if (pt == 0) mbar_arrive(&bars->req_l2);
         }
         if (pt >= 128 && pt < 192) cp_async_wait_all();
-        if (pt == 64) {  // drain what this thread issued (a completed phase returns at once)
-            if (uw_issued >= 0) (void)mbar_wait(&bars->prep_mma[uw_issued & 1], (uw_issued >> 1) & 1);
-            if (gram_issued > gram_waited) (void)mbar_wait(&bars->gram, gram_issued & 1);
-        }
-    } else {
-        // ------------------------------------------------------------ chain
+        if (pt == kGramThread && gram_issued > gram_waited)  // drain (a completed phase returns at once)
+            (void)mbar_wait(&bars->gram, gram_issued & 1);
+    } else if (warp < (kPrep + kChain) / 32) {
+        // ------------------------------------------------------------ chain (serial path)
         const int ct = tid - kPrep;  // dv row = TMEM lane
-        // the first chunks' loads go out before anything else
-        int last_load[kStages];  // last chunk loaded into each stage (thread ct == 32 loads)
-#pragma unroll
-        for (int i = 0; i < kStages; ++i) last_load[i] = -1;
-        if (ct == 32) {
-            tma_prefetch_desc(&tm_q);
-            tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
-            tma_prefetch_desc(&tm_o);
-            for (int c = 0; c < kStages && c < n_chunks; ++c) {
-                load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, c, bhk, bh);
-                last_load[c] = c;
-            }
-            if (n_chunks > kStages) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, kStages, bhk, bh);
-        }
         // S^T (fp32) and its bf16 copy (the A operand of each chunk's first product) into TMEM
         auto store_state_bf16 = [&](int half, const float* x64) {
             uint32_t u[32];
@@ -629,32 +603,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_before();
         named_bar_sync(BAR_CHAIN, kChain);
-        int issued1 = -1, issued23 = -1;  // last chunk whose chain MMAs were committed
+        int issued0 = -1, issued1 = -1, issued2 = -1;  // last chunk whose U/W, first, state products were committed
         bool ok = true;
         for (int c = 0; c < n_chunks && ok; ++c) {
             const int s = c % kStages;  // input stage
             const int db = c & 1;       // TMEM buffer R_D
             const uint32_t st_s = sbase + s * STAGE_BYTES;
-            uint8_t* st = sm + s * STAGE_BYTES;
-            // ---- chunk c from prep, and its U/W product
-            bool fail = !mbar_wait_or_abort(&bars->ready[s], (c / kStages) & 1, abort_flag);
-            if (!fail) fail = !mbar_wait_or_abort(&bars->prep_mma[db], (c >> 1) & 1, abort_flag);
-            tc_fence_after();
-            if (!fail) {
-                // -W over V (the U product has read V), K-major: dk on the rows' elements, tokens
-                // on the rows; then the output half of R_D[db] is zeroed for the accumulation below
-                const uint32_t waddr = trow + COL_D + 128 * db + 64;
-                tmem_store_transposed(waddr, st + ST_VW0, ST_HALF, (warp & 3) * 32, -1.f, lane);
-                float z[32];
+            bool fail = false;
+            if (ct == 0) {
+                // ---- [U^T | W^T] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T] into R_D[db], once
+                //      prep has written the solve's operands and the helpers have read chunk c - 2's
+                //      output from that buffer (issued here: this thread waits for its result anyway)
+                fail = !mbar_wait_or_abort(&bars->req_l2, c & 1, abort_flag);
+                if (!fail && c >= 2) fail = !mbar_wait_or_abort(&bars->dfree[db], ((c - 2) >> 1) & 1, abort_flag);
+                if (!fail) {
+                    tc_fence_after();
 #pragma unroll
-                for (int i = 0; i < 32; ++i) z[i] = 0.f;
-                tmem_st32(waddr, z);
-                tmem_st32(waddr + 32, z);
-                tmem_wait_st();
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_D + 128 * db, make_sdesc(st_s + ST_VW0 + kk * 2048, ST_HALF, 1024),
+                                 make_sdesc(sbase + OFF_T12 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
+                                 make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+                    mma_commit(&bars->prep_mma[db]);
+                    issued0 = c;
+                }
             }
-            fence_proxy_async_smem();
-            tc_fence_before();
-            if (ct == 0) tma_store_wait_read0();  // the out tile of chunk c - 2 has been read
+            // ---- chunk c from prep (Q', P) and its -W from the helper warps
+            if (!fail) fail = !mbar_wait_or_abort(&bars->ready[s], (c / kStages) & 1, abort_flag);
+            if (!fail) fail = !mbar_wait_or_abort(&bars->w_ready, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             if (ct == 0) {
                 tc_fence_after();
@@ -681,78 +659,51 @@ __global__ void __launch_bounds__(kThreads, 1)
                     tmem_st32(trow + COL_S + c0, x);
                 }
                 tmem_wait_st();
-            } else {
-                // output of the previous chunk (its accumulator completed before the barrier that
-                // ended the previous iteration) while the product runs; prep may then reuse the buffer
-                tc_fence_after();
-                tmem_store_transposed(trow + COL_D + 128 * ((c - 1) & 1) + 64, sm + OFF_OUT, 8192, (warp & 3) * 32,
-                                      scale, lane);
-                tc_fence_before();
-                mbar_arrive(&bars->dfree[(c - 1) & 1]);
-                fence_proxy_async_smem();
             }
             fail = !mbar_wait_or_abort(&bars->c1, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             tc_fence_after();
-            // Delta^T as a K-major bf16 operand over [-W; Q'] (dk 0..63), and Delta^T diag(exp(G_C - G))
-            // over [-W; Q'] (dk 64..127), both consumed by the product above
+            // Delta^T (fp32, columns 0..63 of R_D[db]) becomes two bf16 A operands, one 32-bit
+            // column per token pair (even token in the low half): Delta^T in place in columns
+            // 0..31, and Delta^T diag(exp(G_C - G)) in the bf16-state columns, free from the
+            // completion of the first product until the state copy is taken again below
             {
                 const float* ec = sEcs + 64 * (c & 3);
-                float x[2][32];
-                tmem_ld32(trow + COL_D + 128 * db, x[0]);
-                tmem_ld32(trow + COL_D + 128 * db + 32, x[1]);
-                tmem_wait_ld();
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    st_row_bf16x32(st + ST_DT, ct, 64 * h, x[h]);
+                for (int h = 0; h < 2; ++h) {  // tokens 32 h .. 32 h + 31 (columns already read are rewritten)
+                    float x[32];
+                    tmem_ld32(trow + COL_D + 128 * db + 32 * h, x);
+                    tmem_wait_ld();
+                    uint32_t u[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) u[j] = pack_bf16x2(x[2 * j], x[2 * j + 1]);
+                    tmem_st16u(trow + COL_D + 128 * db + 16 * h, u);
 #pragma unroll
                     for (int q = 0; q < 8; ++q) {
                         const float4 e = *reinterpret_cast<const float4*>(ec + 32 * h + 4 * q);
-                        x[h][4 * q] *= e.x;
-                        x[h][4 * q + 1] *= e.y;
-                        x[h][4 * q + 2] *= e.z;
-                        x[h][4 * q + 3] *= e.w;
+                        u[2 * q] = pack_bf16x2(x[4 * q] * e.x, x[4 * q + 1] * e.y);
+                        u[2 * q + 1] = pack_bf16x2(x[4 * q + 2] * e.z, x[4 * q + 3] * e.w);
                     }
-                    st_row_bf16x32(st + ST_DT2, ct, 64 * h, x[h]);
+                    tmem_st16u(trow + COL_SA + 16 * h, u);
                 }
+                tmem_wait_st();
             }
-            fence_proxy_async_smem();
             tc_fence_before();
             named_bar_sync(BAR_CHAIN, kChain);
             if (ct == 0) {
+                mbar_arrive(&bars->dt_ready);  // the helper warps issue the output product
                 tc_fence_after();
-                // S^T += (Delta^T diag(exp(G_C - G))) K
+                // S^T += (Delta^T diag(exp(G_C - G))) K  (A from TMEM)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_S, make_sdesc(st_s + ST_DT2 + kk * 32, 16, 1024),
-                             make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024), IDESC_N128_KM, 1);
+                    mma_bf16_tmem_a(tmem + COL_S, tmem + COL_SA + 8 * kk,
+                                    make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024), IDESC_N128_KM, 1);
                 mma_commit(&bars->c2);
-                // O^T += Delta^T P^T
-#pragma unroll
-                for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_DT + kk * 32, 16, 1024),
-                             make_sdesc(st_s + ST_P + kk * 32, 16, 1024), IDESC_N64_KK, 1);
-                mma_commit(&bars->c3);
-                if (c >= 1) {  // out tile of chunk c - 1
-                    tma_store_3d(&tm_o, sm + OFF_OUT, 0, (c - 1) * kC, bh);
-                    tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, (c - 1) * kC, bh);
-                    tma_store_commit();
-                }
             }
-            issued23 = c;
+            issued2 = c;
             fail = !mbar_wait_or_abort(&bars->c2, c & 1, abort_flag);
             if (named_bar_any(BAR_CHAIN, kChain, fail)) { ok = false; break; }
             tc_fence_after();
-            if (ct == 32) {
-                // once the output product has completed, every read of this stage is done:
-                // reload it with chunk c + kStages and prefetch the chunk after into L2
-                // (a failed wait has set the abort flag, which every role checks)
-                if (mbar_wait_or_abort(&bars->c3, c & 1, abort_flag) && c + kStages < n_chunks) {
-                    load_chunk(st, &bars->full[s], &tm_q, &tm_k, &tm_v, c + kStages, bhk, bh);
-                    last_load[s] = c + kStages;
-                    if (c + kStages + 1 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, c + kStages + 1, bhk, bh);
-                }
-            }
             // bf16 copy of the new state for the next chunk's first product, and the state
             // scaled by the next chunk's gamma_C, onto which its increment accumulates
             {
@@ -778,23 +729,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             named_bar_sync(BAR_CHAIN, kChain);
         }
         ok = !named_bar_any(BAR_CHAIN, kChain, !ok || *abort_flag != 0);
-        if (ok && n_chunks > 0) {
-            // output of the last chunk (its product was waited for above), then the final state
-            const int c = n_chunks - 1;
-            if (ct == 0) {
-                tma_store_wait_read0();
-                (void)mbar_wait(&bars->c3, c & 1);  // completed already (waited for inside the loop)
-            }
-            named_bar_sync(BAR_CHAIN, kChain);
+        if (ok && n_chunks > 0) {  // the final state
             tc_fence_after();
-            tmem_store_transposed(trow + COL_D + 128 * (c & 1) + 64, sm + OFF_OUT, 8192, (warp & 3) * 32, scale, lane);
-            fence_proxy_async_smem();
-            named_bar_sync(BAR_CHAIN, kChain);
-            if (ct == 0) {
-                tma_store_3d(&tm_o, sm + OFF_OUT, 0, c * kC, bh);
-                tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, c * kC, bh);
-                tma_store_commit();
-            }
             float* Sg = state + (size_t)bh * kD * kD;
 #pragma unroll 1
             for (int c0 = 0; c0 < kD; c0 += 32) {
@@ -805,19 +741,105 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 32; ++j) Sg[(size_t)(c0 + j) * kD + ct] = x[j];
             }
         }
-        if (!ok) {  // drain what we issued (waiting on a completed phase returns at once)
-            if (ct == 0) {
-                if (issued1 >= 0) (void)mbar_wait(&bars->c1, issued1 & 1);
-                if (issued23 >= 0) {
-                    (void)mbar_wait(&bars->c2, issued23 & 1);
-                    (void)mbar_wait(&bars->c3, issued23 & 1);
+        if (ct == 0) {  // drain what we issued (bounded; a completed phase returns at once)
+            if (issued0 >= 0) (void)mbar_wait(&bars->prep_mma[issued0 & 1], (issued0 >> 1) & 1);
+            if (issued1 >= 0) (void)mbar_wait(&bars->c1, issued1 & 1);
+            if (issued2 >= 0) (void)mbar_wait(&bars->c2, issued2 & 1);
+        }
+    } else {
+        // ------------------------------------------------------------ helpers
+        // Off the serial path: -W of each chunk, the output product, the output tile and its
+        // store, and the input loads.  Thread ht reads TMEM lanes 32 (warp % 4) + ...
+        const int ht = tid - kPrep - kChain;
+        int last_load[kStages];  // last chunk loaded into each stage (thread ht == 0 loads)
+#pragma unroll
+        for (int i = 0; i < kStages; ++i) last_load[i] = -1;
+        if (ht == 0) {
+            tma_prefetch_desc(&tm_q);
+            tma_prefetch_desc(&tm_k);
+            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(&tm_o);
+            for (int c = 0; c < kStages && c < n_chunks; ++c) {
+                load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, c, bhk, bh);
+                last_load[c] = c;
+            }
+            if (n_chunks > kStages) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, kStages, bhk, bh);
+        }
+        int issued3 = -1;  // last chunk whose output product was committed
+        // Iteration c: the output of chunk c - 1 (its product, the tile, the store, the stage
+        // reload), then -W of chunk c.  Chunk c - 1's Delta^T is waited for before chunk c's -W
+        // is announced, so the chain has taken the previous announcement and w_ready never
+        // runs two phases ahead.
+        for (int c = 0; c <= n_chunks; ++c) {
+            bool fail = false;
+            if (c >= 1) {
+                const int p = c - 1, sp = p % kStages, dbp = p & 1;
+                const uint32_t st_p = sbase + sp * STAGE_BYTES;
+                // ---- O^T += Delta^T P^T for chunk p once the chain has written Delta^T
+                fail = !mbar_wait_or_abort(&bars->dt_ready, p & 1, abort_flag);
+                if (!fail && ht == 0) {
+                    tc_fence_after();
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_tmem_a(tmem + COL_D + 128 * dbp + 64, tmem + COL_D + 128 * dbp + 8 * kk,
+                                        make_sdesc(st_p + ST_P + kk * 32, 16, 1024), IDESC_N64_KK, 1);
+                    mma_commit(&bars->c3);
+                    issued3 = p;
+                }
+                // ---- the output of chunk p; its product and the state increment have read
+                //      stage sp for the last time
+                if (!fail) fail = !mbar_wait_or_abort(&bars->c3, p & 1, abort_flag);
+                if (!fail) fail = !mbar_wait_or_abort(&bars->c2, p & 1, abort_flag);
+                if (named_bar_any(BAR_HELP, kHelp, fail)) break;
+                if (ht == 0 && p + kStages < n_chunks) {
+                    // reload the stage with chunk p + kStages and prefetch the chunk after into L2
+                    load_chunk(sm + sp * STAGE_BYTES, &bars->full[sp], &tm_q, &tm_k, &tm_v, p + kStages, bhk, bh);
+                    last_load[sp] = p + kStages;
+                    if (p + kStages + 1 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, p + kStages + 1, bhk, bh);
+                }
+                if (ht == 0) tma_store_wait_read0();  // the out tile of chunk p - 1 has been read
+                named_bar_sync(BAR_HELP, kHelp);
+                tc_fence_after();
+                tmem_store_transposed(trow + COL_D + 128 * dbp + 64, sm + OFF_OUT, 8192, (warp & 3) * 32, scale, lane);
+                tc_fence_before();
+                mbar_arrive(&bars->dfree[dbp]);  // the U/W product may reuse R_D[dbp]
+                fence_proxy_async_smem();
+                named_bar_sync(BAR_HELP, kHelp);
+                if (ht == 0) {
+                    tma_store_3d(&tm_o, sm + OFF_OUT, 0, p * kC, bh);
+                    tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, p * kC, bh);
+                    tma_store_commit();
                 }
             }
-            if (ct == 32)
-                for (int i = 0; i < kStages; ++i)
-                    if (last_load[i] >= 0) (void)mbar_wait(&bars->full[i], (last_load[i] / kStages) & 1);
+            if (c < n_chunks) {
+                const int s = c % kStages, db = c & 1;
+                // ---- -W over V (the U product has read V), K-major: dk on the rows' elements,
+                //      tokens on the rows; then the output half of R_D[db] is zeroed for the
+                //      accumulation of the chain's first product
+                fail = !mbar_wait_or_abort(&bars->prep_mma[db], (c >> 1) & 1, abort_flag);
+                tc_fence_after();
+                if (!fail) {
+                    const uint32_t waddr = trow + COL_D + 128 * db + 64;
+                    tmem_store_transposed(waddr, sm + s * STAGE_BYTES + ST_VW0, ST_HALF, (warp & 3) * 32, -1.f, lane);
+                    float z[32];
+#pragma unroll
+                    for (int i = 0; i < 32; ++i) z[i] = 0.f;
+                    tmem_st32(waddr, z);
+                    tmem_st32(waddr + 32, z);
+                    tmem_wait_st();
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                if (named_bar_any(BAR_HELP, kHelp, fail)) break;
+                mbar_arrive(&bars->w_ready);
+            }
         }
-        if (ct == 0) tma_store_wait_all0();
+        if (ht == 0) {  // drain what we issued (bounded; a completed phase returns at once)
+            if (issued3 >= 0) (void)mbar_wait(&bars->c3, issued3 & 1);
+            for (int i = 0; i < kStages; ++i)
+                if (last_load[i] >= 0) (void)mbar_wait(&bars->full[i], (last_load[i] / kStages) & 1);
+            tma_store_wait_all0();
+        }
     }
 
     tc_fence_before();

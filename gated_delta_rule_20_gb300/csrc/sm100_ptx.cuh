@@ -64,13 +64,17 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 }
 
 // Wait for the phase with the given parity to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
-    if (mbar_try_wait(bar, parity)) return true;
+// The polling loops are out of line (one copy in the program) and only entered
+// when the first test fails, to keep the inlined code of each wait small.
+__device__ __noinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 255u) == 0 && globaltimer_ns() - t0 > 1000000000ull) return false;
     }
+}
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    return mbar_try_wait(bar, parity) || mbar_wait_loop(bar, parity);
 }
 // As mbar_wait, but also gives up as soon as *abort becomes non-zero (another
 // role of the CTA gave up); a timeout sets *abort itself.
@@ -78,8 +82,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // about 2 us the waiting thread switches to sleeping inside try_wait (up to
 // 20 us per poll) so that long waits leave issue slots and the shared-memory
 // pipe to the warps that are working.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
-    if (mbar_try_wait(bar, parity)) return true;
+__device__ __noinline__ bool mbar_wait_or_abort_loop(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         const bool long_wait = (i > 64) && (globaltimer_ns() - t0 > 2000ull);
@@ -92,6 +95,9 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parit
             }
         }
     }
+}
+__device__ __forceinline__ bool mbar_wait_or_abort(uint64_t* bar, uint32_t parity, volatile int* abort) {
+    return mbar_try_wait(bar, parity) || mbar_wait_or_abort_loop(bar, parity, abort);
 }
 
 // ---------------------------------------------------------------- named barriers
@@ -243,6 +249,14 @@ __device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&r)[3
         "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]),
         "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]),
         "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16u(uint32_t taddr, const uint32_t (&r)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+            taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15])
         : "memory");
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
