@@ -355,7 +355,7 @@ def run_ours(args, rank, world, local_rank):
         "launch_ms": {"median": statistics.median(launch_ms), "min": min(launch_ms), "max": max(launch_ms)},
     }
     if rank == 0 and world == 1:
-        n_seq = args.oracle_sequences
+        n_seq = min(args.oracle_sequences, w.B * w.Hv)
         r = time_oracle(w, n_seq)
         result["cpu_baseline"] = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": r["cores"],
                                   "kind": "oracle",
@@ -400,7 +400,7 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--oracle-sequences", type=int, default=32)
+    ap.add_argument("--oracle-sequences", type=int, default=128)
     ap.add_argument("--reference-sequences", type=int, default=8)
     args = ap.parse_args()
     if args.warmup < 3:
