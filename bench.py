@@ -360,8 +360,9 @@ def run_ours(args, rank, world, local_rank):
         result["cpu_baseline"] = {"value": r["tokens_per_s"], "unit": "tokens/s", "cores": r["cores"],
                                   "kind": "oracle",
                                   "sample": "%d of %d (batch, value-head) sequences, all %d tokens each, "
-                                            "%.1f s wall; scaled to the whole workload" % (
-                                                n_seq, w.B * w.Hv, w.S, r["seconds"])}
+                                            "%.1f s wall%s" % (
+                                                n_seq, w.B * w.Hv, w.S, r["seconds"],
+                                                "" if n_seq == w.B * w.Hv else "; scaled to the whole workload")}
     return result
 
 

@@ -751,9 +751,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Off the serial path: -W of each chunk, the output product, the output tile and its
         // store, and the input loads.  Thread ht reads TMEM lanes 32 (warp % 4) + ...
         const int ht = tid - kPrep - kChain;
-        int last_load[kStages];  // last chunk loaded into each stage (thread ht == 0 loads)
-#pragma unroll
-        for (int i = 0; i < kStages; ++i) last_load[i] = -1;
+        int last_load = -1;  // chunks are loaded in order; this is the last one (thread ht == 0 loads)
         if (ht == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
@@ -761,7 +759,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_o);
             for (int c = 0; c < kStages && c < n_chunks; ++c) {
                 load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, c, bhk, bh);
-                last_load[c] = c;
+                last_load = c;
             }
             if (n_chunks > kStages) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, kStages, bhk, bh);
         }
@@ -794,7 +792,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (ht == 0 && p + kStages < n_chunks) {
                     // reload the stage with chunk p + kStages and prefetch the chunk after into L2
                     load_chunk(sm + sp * STAGE_BYTES, &bars->full[sp], &tm_q, &tm_k, &tm_v, p + kStages, bhk, bh);
-                    last_load[sp] = p + kStages;
+                    last_load = p + kStages;
                     if (p + kStages + 1 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, p + kStages + 1, bhk, bh);
                 }
                 if (ht == 0) tma_store_wait_read0();  // the out tile of chunk p - 1 has been read
@@ -836,8 +834,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ht == 0) {  // drain what we issued (bounded; a completed phase returns at once)
             if (issued3 >= 0) (void)mbar_wait(&bars->c3, issued3 & 1);
-            for (int i = 0; i < kStages; ++i)
-                if (last_load[i] >= 0) (void)mbar_wait(&bars->full[i], (last_load[i] / kStages) & 1);
+            for (int k = last_load - kStages + 1; k <= last_load; ++k)  // the last load of each stage
+                if (k >= 0) (void)mbar_wait(&bars->full[k % kStages], (k / kStages) & 1);
             tma_store_wait_all0();
         }
     }

@@ -78,15 +78,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 }
 // As mbar_wait, but also gives up as soon as *abort becomes non-zero (another
 // role of the CTA gave up); a timeout sets *abort itself.
-// Short waits poll (try_wait without a suspend hint returns quickly); after
-// about 2 us the waiting thread switches to sleeping inside try_wait (up to
-// 20 us per poll) so that long waits leave issue slots and the shared-memory
-// pipe to the warps that are working.
+// The thread polls (try_wait without a suspend hint blocks for a short,
+// hardware-chosen time per test): resuming from a suspended try_wait was
+// measured to cost more than the polling does.
 __device__ __noinline__ bool mbar_wait_or_abort_loop(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
-        const bool long_wait = (i > 64) && (globaltimer_ns() - t0 > 2000ull);
-        if (long_wait ? mbar_try_wait_sleep(bar, parity, 20000u) : mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (*abort) return false;
             if (globaltimer_ns() - t0 > 1000000000ull) {
