@@ -106,3 +106,63 @@ def make_inputs(w: Workload, device="cpu", pin: bool = False):
             t = t.to(device)
         out[key] = t
     return out
+
+
+# ------------------------------------------------------------------ conv1d
+# The depthwise causal conv1d + SiLU in front of the recurrence ("GDN Conv1D
+# Kernel API Reference").  Its channels are q|k|v packed: C = 2 * Hk * Dk +
+# Hv * Dv = 8192 for the Hk = 16, Hv = 32, D = 128 heads above, with K = 4 taps.
+# Recipe (one generator per workload, drawn on the CPU in this order):
+#   mixed / x  ~ N(0, 1) [B, C, T], rounded to the activation dtype;
+#   weight     ~ U(-1/sqrt(K), 1/sqrt(K)) fp32 [C, K] (a depthwise Conv1d's
+#                default initialisation bound for a fan-in of K);
+#   conv_state ~ N(0, 1) [B, C, K] in the activation dtype (decode only).
+
+@dataclasses.dataclass(frozen=True)
+class ConvWorkload:
+    name: str
+    kind: str            # "prefill" or "decode"
+    B: int
+    C: int
+    T: int               # tokens (1 for the decode step)
+    K: int               # taps
+    dtype: str           # activation dtype of mixed / out / conv_state: "f32" or "bf16"
+    seed: int
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def tokens(self) -> int:
+        return self.B * self.T
+
+    def with_(self, **kw) -> "ConvWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+CONV_PREFILL = ConvWorkload("conv1d_prefill_b4_c8192_t4096_k4_bf16", "prefill", 4, 8192, 4096, 4, "bf16", 5)
+CONV_DECODE = ConvWorkload("conv1d_decode_b64_c8192_k4_bf16", "decode", 64, 8192, 1, 4, "bf16", 6)
+
+
+def make_conv_inputs(w: ConvWorkload, device="cpu", pin: bool = False):
+    """Draw a conv1d workload's tensors: x [B, C, T], weight [C, K] fp32 and,
+    for the decode step, conv_state [B, C, K]."""
+    gen = torch.Generator(device="cpu").manual_seed(w.seed)
+    x = torch.randn((w.B, w.C, w.T), generator=gen, dtype=torch.float32).to(w.torch_dtype)
+    bound = 1.0 / math.sqrt(w.K)
+    weight = (torch.rand((w.C, w.K), generator=gen, dtype=torch.float32) * 2.0 - 1.0) * bound
+    state = None
+    if w.kind == "decode":
+        state = torch.randn((w.B, w.C, w.K), generator=gen, dtype=torch.float32).to(w.torch_dtype)
+    out = dict(x=x, weight=weight, state=state)
+    for key in ("x", "weight", "state"):
+        t = out[key]
+        if t is None:
+            continue
+        if pin:
+            t = t.pin_memory()
+        if device != "cpu":
+            t = t.to(device)
+        out[key] = t
+    return out
