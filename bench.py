@@ -35,6 +35,8 @@ PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.md")
 KERNEL_SOURCES = {
     "gdn_prefill_tc_kernel": "gated_delta_rule_20_gb300/csrc/prefill_tc.cu",
     "gdn_decode_kernel": "gated_delta_rule_20_gb300/csrc/decode.cu",
+    "conv1d_prefill_vec8_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
+    "conv1d_decode_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
 }
 
 
@@ -55,6 +57,15 @@ def prefill_flops(w, C=64) -> float:
     per value-head token 6 Dk Dv + C (3 Dk + 2 Dv) + C^2 / 3."""
     per = 6 * w.Dk * w.Dv + C * (3 * w.Dk + 2 * w.Dv) + C * C / 3.0
     return per * w.B * w.Hv * w.S
+
+
+def conv1d_bytes(w) -> int:
+    """Algorithmic bytes of one conv1d call: x in, out, the fp32 weights, and the
+    conv_state (written by the prefill; read and written by the decode step)."""
+    esz = 2 if w.dtype == "bf16" else 4
+    act = w.B * w.C * w.T * esz
+    state = w.B * w.C * w.K * esz
+    return 2 * act + w.C * w.K * 4 + state * (2 if w.kind == "decode" else 1)
 
 
 def decode_bytes(w) -> int:
@@ -304,7 +315,44 @@ def run_ours(args, rank, world, local_rank):
                            "unit": "GB/s", "frac": dbytes / (dms * 1e-3) / 1e9 / peaks["hbm"],
                            "traffic": recorded_traffic("gdn_decode_kernel"), "kernel": "gdn_decode_kernel",
                            "algorithmic_bytes_per_launch": dbytes}}
-    del xd, dstate, dout, flush
+    del xd, dstate, dout
+
+    # ---------------- conv1d in front of the recurrence: prefill (input > L2) and decode (L2 flushed)
+    conv = {}
+    for wc in (workloads.CONV_PREFILL, workloads.CONV_DECODE):
+        wc = wc.with_(seed=wc.seed + 100 * rank)
+        xc = workloads.make_conv_inputs(wc, device=dev)
+        cout = torch.empty_like(xc["x"])
+        cst = xc["state"] if wc.kind == "decode" else torch.empty((wc.B, wc.C, wc.K), dtype=xc["x"].dtype,
+                                                                   device=dev)
+        if wc.kind == "prefill":
+            call = lambda: gdn.conv1d_prefill(xc["x"], xc["weight"], out=cout, conv_state=cst, stream=stream)
+        else:
+            call = lambda: gdn.conv1d_decode(xc["x"], xc["weight"], cst, out=cout, stream=stream)
+        for _ in range(max(args.warmup, 3)):
+            if wc.kind == "decode":
+                flush.zero_()
+            call()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+        for i in range(args.steps):
+            if wc.kind == "decode":
+                flush.zero_()
+            ev[i][0].record(stream)
+            call()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        cms = statistics.median([a.elapsed_time(b) for a, b in ev])
+        cb = conv1d_bytes(wc)
+        kname = "conv1d_prefill_vec8_kernel" if wc.kind == "prefill" else "conv1d_decode_kernel"
+        conv[wc.kind] = {
+            "workload": wc.name, "ms": cms, "tokens_per_s": wc.B * wc.T / (cms * 1e-3) * world,
+            "l2": "input larger than L2" if wc.kind == "prefill" else "flushed (256 MiB write) before every launch",
+            "roofline": {"bound": "hbm", "achieved": cb / (cms * 1e-3) / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+                         "frac": cb / (cms * 1e-3) / 1e9 / peaks["hbm"], "traffic": recorded_traffic(kname),
+                         "kernel": kname, "algorithmic_bytes_per_launch": cb}}
+        del xc, cout, cst
+    del flush
 
     # ---------------- end to end through the public API from pinned host buffers
     xh = {k: (v.to("cpu").pin_memory() if hasattr(v, "to") and v is not None else v) for k, v in x.items()}
@@ -350,7 +398,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "Hk": w.Hk, "Hv": w.Hv, "S": w.S, "Dk": w.Dk, "Dv": w.Dv,
                    "parallelism": "independent sequences per rank" if world > 1 else "single gpu",
                    "l2": "inputs larger than L2 (%.0f MB per step)" % (pbytes / 1e6)},
-        "roofline": roof, "decode": decode, "e2e": e2e, "clocks": clocks,
+        "roofline": roof, "decode": decode, "conv1d": conv, "e2e": e2e, "clocks": clocks,
         "gpu_launches": args.steps * gdn.kernels_per_call(),
         "launch_ms": {"median": statistics.median(launch_ms), "min": min(launch_ms), "max": max(launch_ms)},
     }

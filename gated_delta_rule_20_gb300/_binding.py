@@ -30,13 +30,18 @@ GDN_FORCE_FFMA = 1 << 1
 
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
-            "gdn_device_status", "gdn_kernels_per_call")
+            "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode")
 
 
 class GdnDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("Hk", ctypes.c_int64), ("Hv", ctypes.c_int64), ("S", ctypes.c_int64),
                 ("Dk", ctypes.c_int64), ("Dv", ctypes.c_int64), ("dtype", ctypes.c_int32),
                 ("flags", ctypes.c_uint32)]
+
+
+class GdnConvDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("C", ctypes.c_int64), ("T", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
 
 
 class GdnError(RuntimeError):
@@ -70,6 +75,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_device_status.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]
         L.gdn_kernels_per_call.restype = ctypes.c_int
         L.gdn_kernels_per_call.argtypes = []
+        for name in ("gdn_conv1d_prefill", "gdn_conv1d_decode"):
+            f = getattr(L, name)
+            f.restype = ctypes.c_int
+            f.argtypes = [vp, fp, vp, vp, ctypes.POINTER(GdnConvDims), vp]
         _lib = L
     return _lib
 
@@ -172,3 +181,62 @@ def device_status(device: int = 0, clear: bool = True) -> int:
 
 def kernels_per_call() -> int:
     return int(lib().gdn_kernels_per_call())
+
+
+def _conv_call(name, a, weight, b, c, dims, stream):
+    torch = _torch()
+    if stream is None:
+        stream = torch.cuda.current_stream(weight.device)
+    with torch.cuda.device(weight.device):
+        code = getattr(lib(), name)(_ptr(a), _ptr(weight), _ptr(b), _ptr(c), ctypes.byref(dims),
+                                    ctypes.c_void_p(stream.cuda_stream))
+    _check(code)
+
+
+def _conv_checks(tensors, dtype):
+    torch = _torch()
+    for nm, t in tensors:
+        if not t.is_cuda:
+            raise ValueError("%s must be a CUDA tensor" % nm)
+        if not t.is_contiguous():
+            raise ValueError("%s must be contiguous" % nm)
+        if nm == "weight":
+            if t.dtype != torch.float32:
+                raise TypeError("weight must be float32")
+        elif t.dtype != dtype:
+            raise TypeError("x, out and conv_state must share the activation dtype")
+
+
+def conv1d_prefill(x, weight, out=None, conv_state=None, *, stream=None):
+    """Depthwise causal conv1d + SiLU over a sequence (``gdn_conv1d_prefill``):
+    x [B,C,T] bf16/fp32, weight [C,K] fp32.  Returns ``(out [B,C,T], conv_state [B,C,K])``,
+    the new conv_state being the last K raw tokens."""
+    torch = _torch()
+    B, C, T = x.shape
+    K = weight.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    if conv_state is None:
+        conv_state = torch.empty((B, C, K), dtype=x.dtype, device=x.device)
+    _conv_checks((("x", x), ("weight", weight), ("out", out), ("conv_state", conv_state)), x.dtype)
+    if tuple(weight.shape) != (C, K) or tuple(out.shape) != (B, C, T) or tuple(conv_state.shape) != (B, C, K):
+        raise ValueError("inconsistent shapes")
+    dims = GdnConvDims(B, C, T, K, _dtype_code(x), 0)
+    _conv_call("gdn_conv1d_prefill", x, weight, out, conv_state, dims, stream)
+    return out, conv_state
+
+
+def conv1d_decode(x, weight, conv_state, out=None, *, stream=None):
+    """One token (``gdn_conv1d_decode``): x [B,C,1], weight [C,K] fp32; ``conv_state``
+    [B,C,K] is shifted in place.  Returns ``(out [B,C,1], conv_state)``."""
+    torch = _torch()
+    B, C, T = x.shape
+    K = weight.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    _conv_checks((("x", x), ("weight", weight), ("out", out), ("conv_state", conv_state)), x.dtype)
+    if tuple(weight.shape) != (C, K) or tuple(out.shape) != (B, C, T) or tuple(conv_state.shape) != (B, C, K):
+        raise ValueError("inconsistent shapes")
+    dims = GdnConvDims(B, C, T, K, _dtype_code(x), 0)
+    _conv_call("gdn_conv1d_decode", x, weight, conv_state, out, dims, stream)
+    return out, conv_state

@@ -119,6 +119,55 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v,
                            float* state_inout, void* out,
                            const gdn_dims* dims, gdn_stream_t stream);
 
+/*
+ * Depthwise causal conv1d + SiLU in front of the recurrence, with its conv_state
+ * ("GDN Conv1D Kernel API Reference": gdn_conv1d_prefill, gdn_conv1d_decode;
+ * Parameters, Returns, Notes).  Every channel is an independent K-tap FIR over
+ * the raw (pre-convolution) q|k|v activations:
+ *
+ *     out[b, c, t] = silu( sum_{m=0}^{K-1} w[c, K-1-m] x[b, c, t-m] ),   silu(z) = z / (1 + e^-z)
+ *
+ * (weight[c, K-1] multiplies the current token, as in a depthwise Conv1d).
+ *
+ *   B >= 0 batch (0: nothing to do);  C >= 1 channels;  T >= 0 tokens for the
+ *   prefill, T == 1 for the decode step;  K in [1, 8] taps (more returns
+ *   GDN_ERR_UNSUPPORTED);  dtype = gdn_dtype of x, out and conv_state; the
+ *   weights are fp32.  flags must be 0.
+ */
+typedef struct {
+    int64_t B, C, T, K;
+    int32_t dtype;   /* gdn_dtype */
+    uint32_t flags;  /* 0 */
+} gdn_conv_dims;
+
+/*
+ * gdn_conv1d_prefill -- the whole sequence, starting from zeros (the prefill
+ * takes no previous window).
+ *   mixed           [B, C, T]  dtype, raw input, tokens contiguous per channel
+ *   conv_weight     [C, K]     fp32
+ *   out             [B, C, T]  dtype, silu(causal conv)
+ *   conv_state_out  [B, C, K]  dtype, the last K raw tokens of mixed,
+ *                   right-aligned behind zeros when T < K (written when T == 0 too)
+ * Pointers must be non-NULL (x and out may be NULL when T == 0 or B == 0) and
+ * aligned to their element size (else GDN_ERR_ALIGN).  bf16 rows with T % 8 == 0
+ * and 16-byte aligned x / out take the vectorised path.
+ */
+gdn_status gdn_conv1d_prefill(const void* mixed, const float* conv_weight, void* out, void* conv_state_out,
+                              const gdn_conv_dims* dims, gdn_stream_t stream);
+
+/*
+ * gdn_conv1d_decode -- one token.
+ *   x                 [B, C, 1]  dtype, the current raw token
+ *   conv_weight       [C, K]     fp32
+ *   conv_state_inout  [B, C, K]  dtype, the previous window; overwritten in place
+ *                     with the shifted window (the previous one without its
+ *                     oldest token, then x)
+ *   out               [B, C, 1]  dtype, silu(sum_k w[c, k] window[k])
+ * dims->T must be 1 (else GDN_ERR_DIMS).
+ */
+gdn_status gdn_conv1d_decode(const void* x, const float* conv_weight, void* conv_state_inout, void* out,
+                             const gdn_conv_dims* dims, gdn_stream_t stream);
+
 /* Device workspace gdn_prefill needs for these dims: always 0 (every kernel
  * keeps its intermediates on chip). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);
@@ -134,7 +183,7 @@ const char* gdn_status_string(gdn_status s);
  */
 gdn_status gdn_device_status(int device, int clear, int32_t* code);
 
-/* Number of kernels one call launches (both entry points launch exactly one). */
+/* Number of kernels one call launches (every entry point launches at most one). */
 int gdn_kernels_per_call(void);
 
 #ifdef __cplusplus

@@ -98,3 +98,32 @@ def test_binding_requires_cuda_tensors():
     with pytest.raises(ValueError):
         gdn.prefill(q, q, q, torch.zeros(1, 1, 4), torch.zeros(1, 1, 4), 1.0, torch.zeros(1, 1, 8, 8),
                     torch.zeros(1, 1, 4, 8))
+
+
+def _conv(L, name, dims, x=0x1000, w=0x2000, st=0x3000, out=0x4000):
+    c = lambda v: ctypes.c_void_p(v) if v is not None else None
+    if name == "gdn_conv1d_prefill":
+        return L.gdn_conv1d_prefill(c(x), c(w), c(out), c(st), ctypes.byref(dims) if dims is not None else None, None)
+    return L.gdn_conv1d_decode(c(x), c(w), c(st), c(out), ctypes.byref(dims) if dims is not None else None, None)
+
+
+@pytest.mark.parametrize("name", ["gdn_conv1d_prefill", "gdn_conv1d_decode"])
+def test_conv1d_argument_checks(L, name):
+    """Host-side checks of the conv1d entry points (they run before any launch, so
+    no GPU is needed): every failure returns its code and launches nothing."""
+    D = lambda B=2, C=16, T=1, K=4, dtype=gdn.GDN_BF16, flags=0: gdn.GdnConvDims(B, C, T, K, dtype, flags)
+    assert _conv(L, name, None) == gdn.GDN_ERR_NULL
+    assert _conv(L, name, D(dtype=7)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _conv(L, name, D(flags=1)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _conv(L, name, D(K=9)) == gdn.GDN_ERR_UNSUPPORTED
+    assert _conv(L, name, D(K=0)) == gdn.GDN_ERR_DIMS
+    assert _conv(L, name, D(C=0)) == gdn.GDN_ERR_DIMS
+    assert _conv(L, name, D(B=-1)) == gdn.GDN_ERR_DIMS
+    assert _conv(L, name, D(), w=None) == gdn.GDN_ERR_NULL
+    assert _conv(L, name, D(), st=None) == gdn.GDN_ERR_NULL
+    assert _conv(L, name, D(), x=None) == gdn.GDN_ERR_NULL
+    assert _conv(L, name, D(), x=0x1001) == gdn.GDN_ERR_ALIGN        # bf16 needs 2-byte alignment
+    assert _conv(L, name, D(dtype=gdn.GDN_F32), out=0x4002) == gdn.GDN_ERR_ALIGN
+    assert _conv(L, name, D(B=0)) == gdn.GDN_OK                      # nothing to do, nothing launched
+    if name == "gdn_conv1d_decode":
+        assert _conv(L, name, D(T=2)) == gdn.GDN_ERR_DIMS             # one token only
