@@ -26,7 +26,9 @@ namespace {
 constexpr int kMaxTaps = 8;
 constexpr int kThreadsPerBlock = 256;
 
-__device__ __forceinline__ float silu(float z) { return z / (1.f + __expf(-z)); }
+// silu(z) = z / (1 + e^-z), with the fast exponential and division (a few ulp of
+// fp32, far inside the outputs' bf16 rounding and the fp32 tolerance).
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T v);
@@ -79,9 +81,10 @@ __device__ __forceinline__ uint4 shfl4(uint4 v, int src) {
                       __shfl_sync(0xffffffffu, v.z, src), __shfl_sync(0xffffffffu, v.w, src));
 }
 
+template <int K>  // taps, 1..8, fixed at compile time
 __global__ void __launch_bounds__(kThreadsPerBlock) conv1d_prefill_vec8_kernel(
     const uint4* __restrict__ x, const float* __restrict__ w, uint4* __restrict__ out,
-    __nv_bfloat16* __restrict__ state, int C, int nvec, int K, int segs_per_row, long long n_warps) {
+    __nv_bfloat16* __restrict__ state, int C, int nvec, int segs_per_row, long long n_warps) {
     const long long wid = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (wid >= n_warps) return;  // whole warps leave together
     const int lane = threadIdx.x & 31;
@@ -96,9 +99,9 @@ __global__ void __launch_bounds__(kThreadsPerBlock) conv1d_prefill_vec8_kernel(
         cur[u] = (v < nvec) ? xr[v] : make_uint4(0u, 0u, 0u, 0u);
     }
     const uint4 head = (lane == 0 && v0 > 0) ? xr[v0 - 1] : make_uint4(0u, 0u, 0u, 0u);
-    float wb[kMaxTaps];  // wb[m] multiplies the token m steps back
+    float wb[K];  // wb[m] multiplies the token m steps back
 #pragma unroll
-    for (int m = 0; m < kMaxTaps; ++m) wb[m] = (m < K) ? w[(long long)c * K + (K - 1 - m)] : 0.f;
+    for (int m = 0; m < K; ++m) wb[m] = w[(long long)c * K + (K - 1 - m)];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
         uint4 prev = shfl_up4(cur[u], 1);
@@ -114,17 +117,26 @@ __global__ void __launch_bounds__(kThreadsPerBlock) conv1d_prefill_vec8_kernel(
             for (int j = 0; j < 8; ++j) {
                 float z = 0.f;
 #pragma unroll
-                for (int m = 0; m < kMaxTaps; ++m) z = fmaf(wb[m], xx[8 + j - m], z);
+                for (int m = 0; m < K; ++m) z = fmaf(wb[m], xx[8 + j - m], z);
                 y[j] = silu(z);
             }
             out[row * nvec + v] =
                 make_uint4(pack2(y[0], y[1]), pack2(y[2], y[3]), pack2(y[4], y[5]), pack2(y[6], y[7]));
             if (v == nvec - 1) {  // the row's last vector holds its last K raw tokens (T >= 8 >= K)
                 const __nv_bfloat16* xv = reinterpret_cast<const __nv_bfloat16*>(xr + v);
+#pragma unroll
                 for (int k = 0; k < K; ++k) state[row * K + k] = xv[8 - K + k];
             }
         }
     }
+}
+
+template <int K>
+void launch_vec8(const void* mixed, const float* w, void* out, void* state, int C, int nvec, int segs,
+                 long long n_warps, unsigned int blocks, cudaStream_t s) {
+    conv1d_prefill_vec8_kernel<K><<<blocks, kThreadsPerBlock, 0, s>>>(
+        static_cast<const uint4*>(mixed), w, static_cast<uint4*>(out), static_cast<__nv_bfloat16*>(state), C, nvec,
+        segs, n_warps);
 }
 
 // Any dtype, T, alignment: one thread per (b, c, t).
@@ -235,9 +247,17 @@ gdn_status gdn_conv1d_prefill(const void* mixed, const float* conv_weight, void*
         const int nvec = T / 8;
         const int segs = (nvec + kSeg - 1) / kSeg;
         const long long n_warps = rows * segs;
-        conv1d_prefill_vec8_kernel<<<blocks_for(n_warps * 32), kThreadsPerBlock, 0, s>>>(
-            static_cast<const uint4*>(mixed), conv_weight, static_cast<uint4*>(out),
-            static_cast<__nv_bfloat16*>(conv_state_out), C, nvec, K, segs, n_warps);
+        const unsigned int blocks = blocks_for(n_warps * 32);
+        switch (K) {
+            case 1: launch_vec8<1>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+            case 2: launch_vec8<2>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+            case 3: launch_vec8<3>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+            case 4: launch_vec8<4>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+            case 5: launch_vec8<5>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+            case 6: launch_vec8<6>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+            case 7: launch_vec8<7>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+            default: launch_vec8<8>(mixed, conv_weight, out, conv_state_out, C, nvec, segs, n_warps, blocks, s); break;
+        }
     } else if (bf16) {
         const long long total = rows * T;
         conv1d_prefill_scalar_kernel<__nv_bfloat16><<<blocks_for(total), kThreadsPerBlock, 0, s>>>(
