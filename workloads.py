@@ -166,3 +166,61 @@ def make_conv_inputs(w: ConvWorkload, device="cpu", pin: bool = False):
             t = t.to(device)
         out[key] = t
     return out
+
+
+# ------------------------------------------------------------------ gated decode step
+# One token of the decode block's gated step: the post-conv q|k|v row, the output
+# gate z, the raw gate inputs a, b and the per-head parameters.  Recipe (one
+# generator per workload, drawn on the CPU in this order):
+#   qkv   ~ N(0, 1) [B, 2 Hk Dk + Hv Dv]  (q, k are normalised by the kernel itself)
+#   z     ~ N(0, 1) [B, Hv Dv];  a ~ N(0, 1), b ~ N(0, 1) [B, Hv]   (activation dtype)
+#   A_log = log(U(1, 16)) [Hv];  dt ~ exp(U(log 1e-3, log 1e-1)), dt_bias = dt + log(1 - e^-dt)
+#           (the inverse softplus of dt) [Hv];  norm_weight = 1 + 0.1 N(0, 1) [Dv]   (fp32)
+#   state ~ N(0, sigma) [B, Hv, Dk, Dv] fp32.
+
+@dataclasses.dataclass(frozen=True)
+class GatedWorkload:
+    name: str
+    B: int
+    Hk: int
+    Hv: int
+    Dk: int
+    Dv: int
+    dtype: str
+    state_std: float
+    seed: int
+
+    @property
+    def torch_dtype(self):
+        return torch.float32 if self.dtype == "f32" else torch.bfloat16
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / math.sqrt(self.Dk)
+
+    def with_(self, **kw) -> "GatedWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+GATED_DECODE = GatedWorkload("gated_decode_b64_hk16_hv32_d128_bf16", 64, 16, 32, 128, 128, "bf16", 0.02, 7)
+
+
+def make_gated_inputs(w: GatedWorkload, device="cpu"):
+    gen = torch.Generator(device="cpu").manual_seed(w.seed)
+    dt = w.torch_dtype
+    rn = lambda *shape: torch.randn(shape, generator=gen, dtype=torch.float32)
+    ru = lambda lo, hi, *shape: torch.rand(shape, generator=gen, dtype=torch.float32) * (hi - lo) + lo
+    qkv = rn(w.B, 2 * w.Hk * w.Dk + w.Hv * w.Dv).to(dt)
+    z = rn(w.B, w.Hv * w.Dv).to(dt)
+    a = rn(w.B, w.Hv).to(dt)
+    b = rn(w.B, w.Hv).to(dt)
+    A_log = torch.log(ru(1.0, 16.0, w.Hv))
+    dtv = torch.exp(ru(math.log(1e-3), math.log(1e-1), w.Hv))
+    dt_bias = dtv + torch.log(-torch.expm1(-dtv))
+    norm_weight = 1.0 + 0.1 * rn(w.Dv)
+    state = rn(w.B, w.Hv, w.Dk, w.Dv) * w.state_std if w.state_std > 0 else None
+    out = dict(qkv=qkv, z=z, a=a, b=b, A_log=A_log, dt_bias=dt_bias, norm_weight=norm_weight, state=state,
+               scale=w.scale)
+    if device != "cpu":
+        out = {k: (v.to(device) if hasattr(v, "to") else v) for k, v in out.items()}
+    return out
