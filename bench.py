@@ -37,6 +37,7 @@ KERNEL_SOURCES = {
     "gdn_decode_kernel": "gated_delta_rule_20_gb300/csrc/decode.cu",
     "conv1d_prefill_vec8_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
     "conv1d_decode_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
+    "gdn_decode_gated_kernel": "gated_delta_rule_20_gb300/csrc/decode_gated.cu",
 }
 
 
@@ -66,6 +67,15 @@ def conv1d_bytes(w) -> int:
     act = w.B * w.C * w.T * esz
     state = w.B * w.C * w.K * esz
     return 2 * act + w.C * w.K * 4 + state * (2 if w.kind == "decode" else 1)
+
+
+def gated_bytes(w) -> int:
+    """Algorithmic bytes of one gated decode step: the fp32 state in and out, the
+    q|k|v row, z and out, a and b, and the per-head parameters."""
+    esz = 2 if w.dtype == "bf16" else 4
+    state = 2 * w.B * w.Hv * w.Dk * w.Dv * 4
+    act = w.B * (2 * w.Hk * w.Dk + w.Hv * w.Dv) * esz + 2 * w.B * w.Hv * w.Dv * esz + 2 * w.B * w.Hv * esz
+    return state + act + 2 * w.Hv * 4 + w.Dv * 4
 
 
 def decode_bytes(w) -> int:
@@ -352,7 +362,36 @@ def run_ours(args, rank, world, local_rank):
                          "frac": cb / (cms * 1e-3) / 1e9 / peaks["hbm"], "traffic": recorded_traffic(kname),
                          "kernel": kname, "algorithmic_bytes_per_launch": cb}}
         del xc, cout, cst
-    del flush
+
+    # ---------------- gated decode step (prologue + recurrence + RMSNormGated), L2 flushed
+    wg = workloads.GATED_DECODE.with_(seed=workloads.GATED_DECODE.seed + 100 * rank)
+    xg = workloads.make_gated_inputs(wg, device=dev)
+    gout = torch.empty((wg.B, wg.Hv * wg.Dv), dtype=wg.torch_dtype, device=dev)
+
+    def gated_step():
+        gdn.decode_gated(xg["qkv"], xg["z"], xg["a"], xg["b"], xg["A_log"], xg["dt_bias"], xg["norm_weight"],
+                         xg["scale"], xg["state"], wg.Hk, wg.Hv, wg.Dk, wg.Dv, out=gout, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        gated_step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        gated_step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    gms = statistics.median([a.elapsed_time(b) for a, b in ev])
+    gb = gated_bytes(wg)
+    gated = {"workload": wg.name, "ms": gms, "value": gb / (gms * 1e-3) / 1e9 * world, "unit": "GB/s",
+             "l2": "flushed (256 MiB write) before every launch",
+             "roofline": {"bound": "hbm", "achieved": gb / (gms * 1e-3) / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+                          "frac": gb / (gms * 1e-3) / 1e9 / peaks["hbm"],
+                          "traffic": recorded_traffic("gdn_decode_gated_kernel"), "kernel": "gdn_decode_gated_kernel",
+                          "algorithmic_bytes_per_launch": gb}}
+    del xg, gout, flush
 
     # ---------------- end to end through the public API from pinned host buffers
     xh = {k: (v.to("cpu").pin_memory() if hasattr(v, "to") and v is not None else v) for k, v in x.items()}
@@ -398,7 +437,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "Hk": w.Hk, "Hv": w.Hv, "S": w.S, "Dk": w.Dk, "Dv": w.Dv,
                    "parallelism": "independent sequences per rank" if world > 1 else "single gpu",
                    "l2": "inputs larger than L2 (%.0f MB per step)" % (pbytes / 1e6)},
-        "roofline": roof, "decode": decode, "conv1d": conv, "e2e": e2e, "clocks": clocks,
+        "roofline": roof, "decode": decode, "decode_gated": gated, "conv1d": conv, "e2e": e2e, "clocks": clocks,
         "gpu_launches": args.steps * gdn.kernels_per_call(),
         "launch_ms": {"median": statistics.median(launch_ms), "min": min(launch_ms), "max": max(launch_ms)},
     }

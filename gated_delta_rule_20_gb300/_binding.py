@@ -30,7 +30,8 @@ GDN_FORCE_FFMA = 1 << 1
 
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
-            "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode")
+            "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
+            "gdn_decode_gated")
 
 
 class GdnDims(ctypes.Structure):
@@ -75,6 +76,9 @@ def lib() -> ctypes.CDLL:
         L.gdn_device_status.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]
         L.gdn_kernels_per_call.restype = ctypes.c_int
         L.gdn_kernels_per_call.argtypes = []
+        L.gdn_decode_gated.restype = ctypes.c_int
+        L.gdn_decode_gated.argtypes = [vp, vp, vp, vp, fp, fp, fp, ctypes.c_float, fp, vp, ctypes.POINTER(GdnDims),
+                                       vp]
         for name in ("gdn_conv1d_prefill", "gdn_conv1d_decode"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -240,3 +244,38 @@ def conv1d_decode(x, weight, conv_state, out=None, *, stream=None):
     dims = GdnConvDims(B, C, T, K, _dtype_code(x), 0)
     _conv_call("gdn_conv1d_decode", x, weight, conv_state, out, dims, stream)
     return out, conv_state
+
+
+def decode_gated(qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state, Hk, Hv, Dk, Dv, out=None, *,
+                 zero_initial_state=False, stream=None):
+    """The gated single-token step (``gdn_decode_gated``): qkv [B, 2 Hk Dk + Hv Dv], z [B, Hv Dv],
+    a, b [B, Hv] in the compute dtype; A_log, dt_bias [Hv], norm_weight [Dv] and ``state``
+    [B, Hv, Dk, Dv] fp32 (updated in place).  Returns ``(out [B, Hv Dv], state)``."""
+    torch = _torch()
+    B = qkv.shape[0]
+    if out is None:
+        out = torch.empty((B, Hv * Dv), dtype=qkv.dtype, device=qkv.device)
+    for nm, t in (("qkv", qkv), ("z", z), ("a", a), ("b", b), ("A_log", A_log), ("dt_bias", dt_bias),
+                  ("norm_weight", norm_weight), ("state", state), ("out", out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % nm)
+    for nm, t in (("z", z), ("a", a), ("b", b), ("out", out)):
+        if t.dtype != qkv.dtype:
+            raise TypeError("%s must share the compute dtype of qkv" % nm)
+    for nm, t in (("A_log", A_log), ("dt_bias", dt_bias), ("norm_weight", norm_weight), ("state", state)):
+        if t.dtype != torch.float32:
+            raise TypeError("%s must be float32" % nm)
+    if tuple(qkv.shape) != (B, 2 * Hk * Dk + Hv * Dv) or tuple(z.shape) != (B, Hv * Dv) or \
+            tuple(a.shape) != (B, Hv) or tuple(b.shape) != (B, Hv) or tuple(A_log.shape) != (Hv,) or \
+            tuple(dt_bias.shape) != (Hv,) or tuple(norm_weight.shape) != (Dv,) or \
+            tuple(state.shape) != (B, Hv, Dk, Dv) or tuple(out.shape) != (B, Hv * Dv):
+        raise ValueError("inconsistent shapes")
+    dims = make_dims(B, Hk, Hv, 1, Dk, Dv, _dtype_code(qkv), GDN_ZERO_INITIAL_STATE if zero_initial_state else 0)
+    if stream is None:
+        stream = torch.cuda.current_stream(qkv.device)
+    with torch.cuda.device(qkv.device):
+        code = lib().gdn_decode_gated(_ptr(qkv), _ptr(z), _ptr(a), _ptr(b), _ptr(A_log), _ptr(dt_bias),
+                                      _ptr(norm_weight), ctypes.c_float(scale), _ptr(state), _ptr(out),
+                                      ctypes.byref(dims), ctypes.c_void_p(stream.cuda_stream))
+    _check(code)
+    return out, state

@@ -1,0 +1,272 @@
+// decode_gated.cu -- the gated single-token step of the decode block: the
+// decode prologue (L2-normalised q and k, the decay g and update strength beta
+// from the raw gate inputs), one token of the recurrence, and the RMSNormGated
+// output epilogue ("GDN Block TKG Kernel API Reference": gdn_block_tkg
+// Parameters A_log, dt_bias, norm_weight and the z / a / b projections,
+// Returns "RMSNormGated decode output"; the data flow into gdn_tkg).
+//
+//     q^ = q / sqrt(|q|^2 + eps_l2),  k^ likewise
+//     g  = -exp(A_log[h]) softplus(a + dt_bias[h]),   beta = sigmoid(b)
+//     p_k = S^T k^,  p_q = S^T q^,  d = beta (v - e^g p_k)
+//     o  = scale (e^g p_q + d (k^ . q^)),   S' = e^g S + k^ d^T   (in place)
+//     y  = o / sqrt(mean_Dv(o^2) + eps_rms) * norm_weight * silu(z)
+//
+// One CTA per (batch, value head) covers all Dv <= 128 columns, because the
+// RMS norm runs over the whole head: 256 threads = 32 column groups of 4 floats
+// x 8 row groups; a warp reads one full 512-byte state row segment per load.
+// Every fp32 state element is read once and written once.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "gdn.h"
+
+namespace gdn {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kColGroups = 32;  // x 4 columns = 128
+constexpr int kRowGroups = 8;
+constexpr int kMaxRows = 128 / kRowGroups;
+constexpr float kEpsL2 = 1e-6f;
+constexpr float kEpsRms = 1e-6f;
+
+template <typename T>
+__device__ __forceinline__ float to_f32(T x);
+template <>
+__device__ __forceinline__ float to_f32<float>(float x) {
+    return x;
+}
+template <>
+__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
+    return __bfloat162float(x);
+}
+template <typename T>
+__device__ __forceinline__ T from_f32(float x);
+template <>
+__device__ __forceinline__ float from_f32<float>(float x) {
+    return x;
+}
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
+    return __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ float warp_sum(float x) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    return x;
+}
+__device__ __forceinline__ float softplus(float x) { return x > 20.f ? x : log1pf(expf(x)); }
+
+struct GatedArgs {
+    const void* qkv;
+    const void* z;
+    const void* a;
+    const void* b;
+    const float* A_log;
+    const float* dt_bias;
+    const float* norm_weight;
+    float scale;
+    float* state;
+    void* out;
+    int Hk, Hv, Dk, Dv, zero_init;
+};
+
+template <typename T, bool kVec>
+__global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs p) {
+    __shared__ float s_k[128], s_q[128];
+    __shared__ float s_red[2][kRowGroups][128];
+    __shared__ float s_d[128];
+    __shared__ float s_part[3][8];  // per-warp partial sums
+    __shared__ float s_scalar[4];   // |q|^2, |k|^2, k.q, sum o^2
+
+    const int bh = blockIdx.x;
+    const int Hv = p.Hv, Dk = p.Dk, Dv = p.Dv;
+    const int b = bh / Hv, h = bh - b * Hv;
+    const int hk = h / (Hv / p.Hk);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int cg = tid & (kColGroups - 1), rg = tid >> 5;
+    const int c0 = cg * 4;
+    const long long conv_dim = 2LL * p.Hk * Dk + (long long)Hv * Dv;
+    const T* row_in = static_cast<const T*>(p.qkv) + b * conv_dim;
+    const T* qp = row_in + (long long)hk * Dk;
+    const T* kp = row_in + (long long)p.Hk * Dk + (long long)hk * Dk;
+    const T* vp = row_in + 2LL * p.Hk * Dk + (long long)h * Dv;
+    float* Sp = p.state + (long long)bh * Dk * Dv;
+
+    // the state loads go out first: they are the bulk of the traffic
+    float4 S[kMaxRows];
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+        const int r = rg + i * kRowGroups;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!p.zero_init && r < Dk) {
+            if (kVec) {
+                if (c0 < Dv) x = __ldcs(reinterpret_cast<const float4*>(Sp + (long long)r * Dv + c0));
+            } else {
+                const float* row = Sp + (long long)r * Dv;
+                if (c0 + 0 < Dv) x.x = row[c0 + 0];
+                if (c0 + 1 < Dv) x.y = row[c0 + 1];
+                if (c0 + 2 < Dv) x.z = row[c0 + 2];
+                if (c0 + 3 < Dv) x.w = row[c0 + 3];
+            }
+        }
+        S[i] = x;
+    }
+
+    // prologue: q, k and their norms; the gates
+    float qv = 0.f, kv = 0.f;
+    if (tid < Dk) {
+        qv = to_f32(qp[tid]);
+        kv = to_f32(kp[tid]);
+    }
+    {
+        const float sq = warp_sum(qv * qv), sk = warp_sum(kv * kv), skq = warp_sum(qv * kv);
+        if (lane == 0) {
+            s_part[0][warp] = sq;
+            s_part[1][warp] = sk;
+            s_part[2][warp] = skq;
+        }
+    }
+    __syncthreads();
+    if (tid < 3) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) t += s_part[tid][w];
+        s_scalar[tid] = t;
+    }
+    __syncthreads();
+    const float inv_q = rsqrtf(s_scalar[0] + kEpsL2), inv_k = rsqrtf(s_scalar[1] + kEpsL2);
+    const float kq = s_scalar[2] * inv_q * inv_k;
+    if (tid < Dk) {
+        s_q[tid] = qv * inv_q;
+        s_k[tid] = kv * inv_k;
+    }
+    const float g = -expf(p.A_log[h]) * softplus(to_f32(static_cast<const T*>(p.a)[bh]) + p.dt_bias[h]);
+    const float decay = expf(g);
+    const float beta = 1.f / (1.f + expf(-to_f32(static_cast<const T*>(p.b)[bh])));
+    __syncthreads();
+
+    // S^T k^ and S^T q^: partials over this thread's rows, then over the row groups
+    float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+        const int r = rg + i * kRowGroups;
+        if (r < Dk) {
+            const float kr = s_k[r], qr = s_q[r];
+            pk[0] = fmaf(S[i].x, kr, pk[0]);
+            pk[1] = fmaf(S[i].y, kr, pk[1]);
+            pk[2] = fmaf(S[i].z, kr, pk[2]);
+            pk[3] = fmaf(S[i].w, kr, pk[3]);
+            pq[0] = fmaf(S[i].x, qr, pq[0]);
+            pq[1] = fmaf(S[i].y, qr, pq[1]);
+            pq[2] = fmaf(S[i].z, qr, pq[2]);
+            pq[3] = fmaf(S[i].w, qr, pq[3]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        s_red[0][rg][c0 + j] = pk[j];
+        s_red[1][rg][c0 + j] = pq[j];
+    }
+    __syncthreads();
+    float o = 0.f;
+    if (tid < Dv) {
+        float sk = 0.f, sq = 0.f;
+#pragma unroll
+        for (int gi = 0; gi < kRowGroups; ++gi) {
+            sk += s_red[0][gi][tid];
+            sq += s_red[1][gi][tid];
+        }
+        const float d = beta * (to_f32(vp[tid]) - decay * sk);
+        s_d[tid] = d;
+        o = p.scale * (decay * sq + d * kq);
+    }
+    // epilogue: RMS of o over the head, gate, store
+    {
+        const float so = warp_sum(o * o);
+        if (lane == 0) s_part[0][warp] = so;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) t += s_part[0][w];
+        s_scalar[3] = t;
+    }
+    __syncthreads();
+    if (tid < Dv) {
+        const float rinv = rsqrtf(s_scalar[3] / (float)Dv + kEpsRms);
+        const float zv = to_f32(static_cast<const T*>(p.z)[(long long)bh * Dv + tid]);
+        const float gate = zv / (1.f + expf(-zv));
+        static_cast<T*>(p.out)[(long long)bh * Dv + tid] = from_f32<T>(o * rinv * p.norm_weight[tid] * gate);
+    }
+
+    // S' = e^g S + k^ d^T, in place
+    const float d0 = s_d[c0 + 0], d1 = s_d[c0 + 1], d2 = s_d[c0 + 2], d3 = s_d[c0 + 3];
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+        const int r = rg + i * kRowGroups;
+        if (r < Dk) {
+            const float kr = s_k[r];
+            float4 x;
+            x.x = fmaf(decay, S[i].x, kr * d0);
+            x.y = fmaf(decay, S[i].y, kr * d1);
+            x.z = fmaf(decay, S[i].z, kr * d2);
+            x.w = fmaf(decay, S[i].w, kr * d3);
+            if (kVec) {
+                if (c0 < Dv) __stcs(reinterpret_cast<float4*>(Sp + (long long)r * Dv + c0), x);
+            } else {
+                float* row = Sp + (long long)r * Dv;
+                if (c0 + 0 < Dv) row[c0 + 0] = x.x;
+                if (c0 + 1 < Dv) row[c0 + 1] = x.y;
+                if (c0 + 2 < Dv) row[c0 + 2] = x.z;
+                if (c0 + 3 < Dv) row[c0 + 3] = x.w;
+            }
+        }
+    }
+}
+
+template <typename T>
+cudaError_t launch_gated(const GatedArgs& a, int B, cudaStream_t s) {
+    const bool vec = (a.Dv % 4) == 0 && (reinterpret_cast<uintptr_t>(a.state) & 15u) == 0;
+    if (vec)
+        gdn_decode_gated_kernel<T, true><<<B * a.Hv, kThreads, 0, s>>>(a);
+    else
+        gdn_decode_gated_kernel<T, false><<<B * a.Hv, kThreads, 0, s>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" gdn_status gdn_decode_gated(const void* qkv, const void* z, const void* a, const void* b,
+                                       const float* A_log, const float* dt_bias, const float* norm_weight,
+                                       float scale, float* state_inout, void* out, const gdn_dims* d,
+                                       gdn_stream_t stream) {
+    if (!d) return GDN_ERR_NULL;
+    if (d->dtype != GDN_F32 && d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
+    if (d->flags & ~(uint32_t)GDN_ZERO_INITIAL_STATE) return GDN_ERR_UNSUPPORTED;
+    if (d->B < 0 || d->Hk < 1 || d->Hv < 1 || d->S != 1 || d->Dk < 1 || d->Dv < 1) return GDN_ERR_DIMS;
+    if (d->Dk > 128 || d->Dv > 128 || d->Hv % d->Hk != 0) return GDN_ERR_DIMS;
+    if (d->B * d->Hv > INT32_MAX) return GDN_ERR_DIMS;
+    if (d->B == 0) return GDN_OK;
+    if (!qkv || !z || !a || !b || !A_log || !dt_bias || !norm_weight || !state_inout || !out) return GDN_ERR_NULL;
+    const uintptr_t esz = d->dtype == GDN_BF16 ? 2 : 4;
+    if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(a) |
+         reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(out)) & (esz - 1))
+        return GDN_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(A_log) | reinterpret_cast<uintptr_t>(dt_bias) |
+         reinterpret_cast<uintptr_t>(norm_weight) | reinterpret_cast<uintptr_t>(state_inout)) & 3u)
+        return GDN_ERR_ALIGN;
+    GatedArgs g{qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state_inout, out,
+                (int)d->Hk, (int)d->Hv, (int)d->Dk, (int)d->Dv, (d->flags & GDN_ZERO_INITIAL_STATE) ? 1 : 0};
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const cudaError_t e = d->dtype == GDN_BF16 ? launch_gated<__nv_bfloat16>(g, (int)d->B, s)
+                                               : launch_gated<float>(g, (int)d->B, s);
+    return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}

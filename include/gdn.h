@@ -120,6 +120,38 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v,
                            const gdn_dims* dims, gdn_stream_t stream);
 
 /*
+ * gdn_decode_gated -- the gated single-token step of the decode block: the
+ * decode prologue, one token of the recurrence, and the RMSNormGated output
+ * epilogue ("GDN Block TKG Kernel API Reference": gdn_block_tkg Parameters
+ * A_log, dt_bias, norm_weight and the z / a / b in_proj outputs; Returns
+ * "RMSNormGated decode output").  The page names these inputs but prints no
+ * formulas; this library reads them as (eps_l2 = eps_rms = 1e-6):
+ *
+ *     q^ = q / sqrt(|q|^2 + eps_l2),  k^ likewise (q and k need NOT be normalised)
+ *     g  = -exp(A_log[h]) * softplus(a[b, h] + dt_bias[h]),   beta = sigmoid(b[b, h])
+ *     (o, S') = the recurrence step of gdn_decode_step on q^, k^, v, g, beta, scale
+ *     y  = o / sqrt(mean over Dv of o^2 + eps_rms) * norm_weight * silu(z)
+ *
+ *   qkv          [B, 2*Hk*Dk + Hv*Dv]  compute dtype: the post-conv q | k | v row
+ *                (q [Hk, Dk] head-major, then k [Hk, Dk], then v [Hv, Dv])
+ *   z            [B, Hv*Dv]  compute dtype, output gate
+ *   a, b         [B, Hv]     compute dtype, raw decay-gate and beta inputs
+ *   A_log, dt_bias [Hv] fp32;  norm_weight [Dv] fp32
+ *   state_inout  [B, Hv, Dk, Dv] fp32, updated in place (GDN_ZERO_INITIAL_STATE
+ *                starts from zeros)
+ *   out          [B, Hv*Dv]  compute dtype, y
+ * dims as for gdn_decode_step (S == 1, Dk, Dv <= 128, Hv % Hk == 0).  Pointers
+ * must be non-NULL and aligned to their element size; the state takes 128-bit
+ * accesses when it is 16-byte aligned and Dv % 4 == 0.
+ */
+#define GDN_L2NORM_EPS 1e-6f
+#define GDN_RMSNORM_EPS 1e-6f
+gdn_status gdn_decode_gated(const void* qkv, const void* z, const void* a, const void* b,
+                            const float* A_log, const float* dt_bias, const float* norm_weight,
+                            float scale, float* state_inout, void* out,
+                            const gdn_dims* dims, gdn_stream_t stream);
+
+/*
  * Depthwise causal conv1d + SiLU in front of the recurrence, with its conv_state
  * ("GDN Conv1D Kernel API Reference": gdn_conv1d_prefill, gdn_conv1d_decode;
  * Parameters, Returns, Notes).  Every channel is an independent K-tap FIR over

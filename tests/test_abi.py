@@ -127,3 +127,21 @@ def test_conv1d_argument_checks(L, name):
     assert _conv(L, name, D(B=0)) == gdn.GDN_OK                      # nothing to do, nothing launched
     if name == "gdn_conv1d_decode":
         assert _conv(L, name, D(T=2)) == gdn.GDN_ERR_DIMS             # one token only
+
+
+def test_decode_gated_argument_checks(L):
+    """Host-side checks of gdn_decode_gated (no launch happens, so no GPU is needed)."""
+    p = ctypes.c_void_p(0x1000)
+    call = lambda d, st=p, a=p: L.gdn_decode_gated(p, p, a, p, p, p, p, ctypes.c_float(1.0), st, p,
+                                                   ctypes.byref(d) if d is not None else None, None)
+    D = lambda **kw: gdn.make_dims(kw.get("B", 2), kw.get("Hk", 2), kw.get("Hv", 4), kw.get("S", 1), kw.get("Dk", 128),
+                                   kw.get("Dv", 128), kw.get("dtype", gdn.GDN_BF16), kw.get("flags", 0))
+    assert call(None) == gdn.GDN_ERR_NULL
+    assert call(D(S=2)) == gdn.GDN_ERR_DIMS
+    assert call(D(Dk=129)) == gdn.GDN_ERR_DIMS
+    assert call(D(Hv=3)) == gdn.GDN_ERR_DIMS
+    assert call(D(dtype=5)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(D(flags=gdn.GDN_FORCE_FFMA)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(D(), st=None) == gdn.GDN_ERR_NULL
+    assert call(D(), a=ctypes.c_void_p(0x1001)) == gdn.GDN_ERR_ALIGN
+    assert call(D(B=0)) == gdn.GDN_OK
