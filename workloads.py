@@ -224,3 +224,61 @@ def make_gated_inputs(w: GatedWorkload, device="cpu"):
     if device != "cpu":
         out = {k: (v.to(device) if hasattr(v, "to") else v) for k, v in out.items()}
     return out
+
+
+# ------------------------------------------------------------------ the decode block
+# The whole decode block without its output projection: the token's hidden state,
+# the four input projections, the conv1d and the gated step.  Hidden size H = 2048.
+# Recipe (one generator, drawn on the CPU in this order):
+#   hidden ~ N(0, 1) [B, 1, H] bf16;  W_qkv, W_z, W_a, W_b ~ N(0, 1/H) bf16 ([H, N], so the
+#   projections are O(1));  conv_weight ~ U(-1/sqrt(K), 1/sqrt(K)) fp32 [C, K];
+#   conv_state ~ N(0, 1) bf16 [B, C, K];  A_log, dt_bias, norm_weight as the gated step;
+#   state ~ N(0, 0.02) fp32.
+
+@dataclasses.dataclass(frozen=True)
+class BlockWorkload:
+    name: str
+    B: int
+    H: int
+    Hk: int
+    Hv: int
+    Dk: int
+    Dv: int
+    K: int
+    seed: int
+
+    @property
+    def C(self) -> int:
+        return 2 * self.Hk * self.Dk + self.Hv * self.Dv
+
+    def with_(self, **kw) -> "BlockWorkload":
+        return dataclasses.replace(self, **kw)
+
+
+DECODE_BLOCK = BlockWorkload("decode_block_b64_h2048_hk16_hv32_d128_k4_bf16", 64, 2048, 16, 32, 128, 128, 4, 8)
+
+
+def make_block_inputs(w: BlockWorkload, device="cpu"):
+    gen = torch.Generator(device="cpu").manual_seed(w.seed)
+    rn = lambda *shape: torch.randn(shape, generator=gen, dtype=torch.float32)
+    ru = lambda lo, hi, *shape: torch.rand(shape, generator=gen, dtype=torch.float32) * (hi - lo) + lo
+    bf = torch.bfloat16
+    sd = 1.0 / math.sqrt(w.H)
+    hidden = rn(w.B, 1, w.H).to(bf)
+    W_qkv = (rn(w.H, w.C) * sd).to(bf)
+    W_z = (rn(w.H, w.Hv * w.Dv) * sd).to(bf)
+    W_a = (rn(w.H, w.Hv) * sd).to(bf)
+    W_b = (rn(w.H, w.Hv) * sd).to(bf)
+    bound = 1.0 / math.sqrt(w.K)
+    conv_weight = (torch.rand((w.C, w.K), generator=gen, dtype=torch.float32) * 2.0 - 1.0) * bound
+    conv_state = rn(w.B, w.C, w.K).to(bf)
+    A_log = torch.log(ru(1.0, 16.0, w.Hv))
+    dtv = torch.exp(ru(math.log(1e-3), math.log(1e-1), w.Hv))
+    dt_bias = dtv + torch.log(-torch.expm1(-dtv))
+    norm_weight = 1.0 + 0.1 * rn(w.Dv)
+    state = rn(w.B, w.Hv, w.Dk, w.Dv) * 0.02
+    out = dict(hidden=hidden, W_qkv=W_qkv, W_z=W_z, W_a=W_a, W_b=W_b, conv_weight=conv_weight,
+               conv_state=conv_state, A_log=A_log, dt_bias=dt_bias, norm_weight=norm_weight, state=state)
+    if device != "cpu":
+        out = {k: v.to(device) for k, v in out.items()}
+    return out
