@@ -38,6 +38,7 @@ KERNEL_SOURCES = {
     "conv1d_prefill_vec8_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
     "conv1d_decode_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
     "gdn_decode_gated_kernel": "gated_delta_rule_20_gb300/csrc/decode_gated.cu",
+    "inproj_gemm_kernel": "gated_delta_rule_20_gb300/csrc/block.cu",
 }
 
 
@@ -76,6 +77,16 @@ def gated_bytes(w) -> int:
     state = 2 * w.B * w.Hv * w.Dk * w.Dv * 4
     act = w.B * (2 * w.Hk * w.Dk + w.Hv * w.Dv) * esz + 2 * w.B * w.Hv * w.Dv * esz + 2 * w.B * w.Hv * esz
     return state + act + 2 * w.Hv * 4 + w.Dv * 4
+
+
+def block_bytes(w) -> int:
+    """Algorithmic bytes of one decode-block call: the four bf16 in_proj weights, the
+    hidden row, the conv window and the fp32 state (each in and out), the conv
+    weights, the per-head parameters and the output."""
+    vd = w.Hv * w.Dv
+    weights = w.H * (w.C + vd + 2 * w.Hv) * 2
+    return (weights + w.B * w.H * 2 + 2 * w.B * w.C * w.K * 2 + 2 * w.B * w.Hv * w.Dk * w.Dv * 4 +
+            w.C * w.K * 4 + 2 * w.Hv * 4 + w.Dv * 4 + w.B * vd * 2)
 
 
 def decode_bytes(w) -> int:
@@ -391,7 +402,40 @@ def run_ours(args, rank, world, local_rank):
                           "frac": gb / (gms * 1e-3) / 1e9 / peaks["hbm"],
                           "traffic": recorded_traffic("gdn_decode_gated_kernel"), "kernel": "gdn_decode_gated_kernel",
                           "algorithmic_bytes_per_launch": gb}}
-    del xg, gout, flush
+    del xg, gout
+
+    # ---------------- the decode block (in_proj GEMM + conv1d decode + gated step), L2 flushed
+    wb = workloads.DECODE_BLOCK.with_(seed=workloads.DECODE_BLOCK.seed + 100 * rank)
+    xb = workloads.make_block_inputs(wb, device=dev)
+    bws = torch.empty(gdn.decode_block_workspace_bytes(wb.B, wb.H, wb.Hk, wb.Hv, wb.Dk, wb.Dv, wb.K),
+                      dtype=torch.uint8, device=dev)
+    bout = torch.empty((wb.B, 1, wb.Hv * wb.Dv), dtype=torch.bfloat16, device=dev)
+
+    def block_step():
+        gdn.decode_block(xb["hidden"], xb["W_qkv"], xb["W_z"], xb["W_a"], xb["W_b"], xb["conv_weight"],
+                         xb["conv_state"], xb["A_log"], xb["dt_bias"], xb["norm_weight"], xb["state"], wb.Hk, wb.Hv,
+                         wb.Dk, wb.Dv, out=bout, workspace=bws, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        flush.zero_()
+        block_step()
+    torch.cuda.synchronize()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        block_step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    bms = statistics.median([a.elapsed_time(b) for a, b in ev])
+    bb = block_bytes(wb)
+    block = {"workload": wb.name, "ms": bms, "tokens_per_s": wb.B / (bms * 1e-3) * world, "kernels": 3,
+             "l2": "flushed (256 MiB write) before every call",
+             "roofline": {"bound": "hbm", "achieved": bb / (bms * 1e-3) / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
+                          "frac": bb / (bms * 1e-3) / 1e9 / peaks["hbm"], "traffic": None,
+                          "kernel": "inproj_gemm_kernel + conv1d_decode_k4_kernel + gdn_decode_gated_kernel",
+                          "algorithmic_bytes_per_call": bb}}
+    del xb, bws, bout, flush
 
     # ---------------- end to end through the public API from pinned host buffers
     xh = {k: (v.to("cpu").pin_memory() if hasattr(v, "to") and v is not None else v) for k, v in x.items()}
@@ -437,7 +481,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "Hk": w.Hk, "Hv": w.Hv, "S": w.S, "Dk": w.Dk, "Dv": w.Dv,
                    "parallelism": "independent sequences per rank" if world > 1 else "single gpu",
                    "l2": "inputs larger than L2 (%.0f MB per step)" % (pbytes / 1e6)},
-        "roofline": roof, "decode": decode, "decode_gated": gated, "conv1d": conv, "e2e": e2e, "clocks": clocks,
+        "roofline": roof, "decode": decode, "decode_gated": gated, "decode_block": block, "conv1d": conv, "e2e": e2e, "clocks": clocks,
         "gpu_launches": args.steps * gdn.kernels_per_call(),
         "launch_ms": {"median": statistics.median(launch_ms), "min": min(launch_ms), "max": max(launch_ms)},
     }

@@ -31,7 +31,7 @@ GDN_FORCE_FFMA = 1 << 1
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
             "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
-            "gdn_decode_gated")
+            "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block")
 
 
 class GdnDims(ctypes.Structure):
@@ -43,6 +43,12 @@ class GdnDims(ctypes.Structure):
 class GdnConvDims(ctypes.Structure):
     _fields_ = [("B", ctypes.c_int64), ("C", ctypes.c_int64), ("T", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("dtype", ctypes.c_int32), ("flags", ctypes.c_uint32)]
+
+
+class GdnBlockDims(ctypes.Structure):
+    _fields_ = [("B", ctypes.c_int64), ("H", ctypes.c_int64), ("Hk", ctypes.c_int64), ("Hv", ctypes.c_int64),
+                ("Dk", ctypes.c_int64), ("Dv", ctypes.c_int64), ("K", ctypes.c_int64), ("dtype", ctypes.c_int32),
+                ("flags", ctypes.c_uint32)]
 
 
 class GdnError(RuntimeError):
@@ -79,6 +85,11 @@ def lib() -> ctypes.CDLL:
         L.gdn_decode_gated.restype = ctypes.c_int
         L.gdn_decode_gated.argtypes = [vp, vp, vp, vp, fp, fp, fp, ctypes.c_float, fp, vp, ctypes.POINTER(GdnDims),
                                        vp]
+        L.gdn_decode_block_workspace_bytes.restype = ctypes.c_size_t
+        L.gdn_decode_block_workspace_bytes.argtypes = [ctypes.POINTER(GdnBlockDims)]
+        L.gdn_decode_block.restype = ctypes.c_int
+        L.gdn_decode_block.argtypes = [vp, vp, vp, vp, vp, fp, vp, fp, fp, fp, fp, vp, vp, ctypes.c_size_t,
+                                       ctypes.POINTER(GdnBlockDims), vp]
         for name in ("gdn_conv1d_prefill", "gdn_conv1d_decode"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -279,3 +290,38 @@ def decode_gated(qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state, Hk, Hv
                                       ctypes.byref(dims), ctypes.c_void_p(stream.cuda_stream))
     _check(code)
     return out, state
+
+
+def decode_block_workspace_bytes(B, H, Hk, Hv, Dk, Dv, K) -> int:
+    return int(lib().gdn_decode_block_workspace_bytes(ctypes.byref(GdnBlockDims(B, H, Hk, Hv, Dk, Dv, K, GDN_BF16, 0))))
+
+
+def decode_block(hidden, W_qkv, W_z, W_a, W_b, conv_weight, conv_state, A_log, dt_bias, norm_weight, state,
+                 Hk, Hv, Dk, Dv, out=None, workspace=None, *, stream=None):
+    """One token through the decode block (``gdn_decode_block``): hidden [B, 1, H] bf16, the four
+    in_proj weights [H, N] bf16, conv_weight [C, K] fp32; ``conv_state`` [B, C, K] bf16 and ``state``
+    [B, Hv, Dk, Dv] fp32 are updated in place.  ``workspace`` (uint8, optional) must hold
+    ``decode_block_workspace_bytes`` bytes.  Returns ``(out [B, 1, Hv Dv], conv_state, state)``."""
+    torch = _torch()
+    B, _, H = hidden.shape
+    K = conv_weight.shape[1]
+    dims = GdnBlockDims(B, H, Hk, Hv, Dk, Dv, K, _dtype_code(hidden), 0)
+    need = int(lib().gdn_decode_block_workspace_bytes(ctypes.byref(dims)))
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=hidden.device)
+    if out is None:
+        out = torch.empty((B, 1, Hv * Dv), dtype=hidden.dtype, device=hidden.device)
+    for nm, t in (("hidden", hidden), ("W_qkv", W_qkv), ("W_z", W_z), ("W_a", W_a), ("W_b", W_b),
+                  ("conv_weight", conv_weight), ("conv_state", conv_state), ("A_log", A_log), ("dt_bias", dt_bias),
+                  ("norm_weight", norm_weight), ("state", state), ("out", out), ("workspace", workspace)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % nm)
+    if stream is None:
+        stream = torch.cuda.current_stream(hidden.device)
+    with torch.cuda.device(hidden.device):
+        code = lib().gdn_decode_block(_ptr(hidden), _ptr(W_qkv), _ptr(W_z), _ptr(W_a), _ptr(W_b), _ptr(conv_weight),
+                                      _ptr(conv_state), _ptr(A_log), _ptr(dt_bias), _ptr(norm_weight), _ptr(state),
+                                      _ptr(out), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                                      ctypes.byref(dims), ctypes.c_void_p(stream.cuda_stream))
+    _check(code)
+    return out, conv_state, state

@@ -1,0 +1,305 @@
+// block.cu -- the decode block without its output projection ("GDN Block TKG
+// Kernel API Reference": gdn_block_tkg Parameters, Returns, Notes and the data
+// flow "in_proj matmuls -> gdn_conv1d_decode -> split conv_out + GQA-repeat q,k
+// -> gdn_tkg").  Three launches on the caller's stream:
+//
+//   1. the four input projections of the token's hidden state, one grouped
+//      tcgen05 GEMM (this file): [B, H] x [H, N] for N = conv_dim, value_dim,
+//      num_v_heads, num_v_heads, written to the caller's workspace in bf16;
+//   2. gdn_conv1d_decode on the q|k|v projection (conv1d.cu);
+//   3. gdn_decode_gated on the conv output, z, a and b (decode_gated.cu).
+//
+// The GEMM is a weight stream (M = B tokens is small): each CTA owns 128 output
+// columns of one weight matrix and runs over H in 64-row slabs.  The product is
+// issued transposed, D^T[n][b] = sum_h W[h][n] X[b][h], so the 128 columns sit on
+// the tcgen05 M / TMEM-lane axis and the batch on N: A = the W slab (MN-major,
+// two 64-column boxes with the 128-byte swizzle), B = the hidden rows (K-major).
+// Warp 0 issues the TMA loads through kGStages stages, warp 1 the MMAs, warps
+// 2..5 write the fp32 accumulator back as bf16 (one TMEM lane quadrant each).
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <mutex>
+
+#include "gdn_internal.h"
+#include "sm100_ptx.cuh"
+
+namespace gdn {
+namespace {
+
+using namespace ptx;
+
+constexpr int kGTile = 128;   // output columns per CTA
+constexpr int kSlab = 64;     // hidden rows per stage
+constexpr int kGStages = 4;
+constexpr int kGThreads = 192;
+constexpr uint32_t kBoxBytes = 64 * 128;  // [64 rows][64 bf16]
+constexpr int kMaxGroups = 4;
+
+struct GemmArgs {
+    void* out[kMaxGroups];        // [B][N_g] bf16
+    int N[kMaxGroups];
+    int tile_start[kMaxGroups + 1];
+    int B, H, nb, npad;           // nb = hidden boxes of 64 rows; npad = MMA N
+    uint32_t stage_bytes, tmem_cols, idesc;
+    int32_t* status;
+};
+
+struct GemmBars {
+    uint64_t full[kGStages];
+    uint64_t empty[kGStages];
+    uint64_t done;
+    uint32_t tmem_base;
+    int abort;
+};
+
+__global__ void __launch_bounds__(kGThreads, 1)
+    inproj_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
+                       const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
+                       const __grid_constant__ CUtensorMap tm_w3, const GemmArgs args) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(sm);
+    GemmBars* bars = reinterpret_cast<GemmBars*>(sm + kGStages * args.stage_bytes);
+    volatile int* abort_flag = &bars->abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    int g = 0;  // weight matrix of this CTA
+    while (g + 1 < kMaxGroups && (int)blockIdx.x >= args.tile_start[g + 1]) ++g;
+    const int n0 = ((int)blockIdx.x - args.tile_start[g]) * kGTile;
+    const CUtensorMap* tm_w = g == 0 ? &tm_w0 : g == 1 ? &tm_w1 : g == 2 ? &tm_w2 : &tm_w3;
+    const int n_slabs = args.H / kSlab;
+
+    if (tid == 0) {
+        for (int s = 0; s < kGStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        mbar_init(&bars->done, 1);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, args.tmem_cols);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {  // TMA producer
+            tma_prefetch_desc(&tm_x);
+            tma_prefetch_desc(tm_w);
+            int loaded = 0;
+            for (int i = 0; i < n_slabs; ++i) {
+                const int s = i % kGStages;
+                if (i >= kGStages && !mbar_wait_or_abort(&bars->empty[s], ((i / kGStages) - 1) & 1, abort_flag)) break;
+                uint8_t* st = sm + s * args.stage_bytes;
+                mbar_arrive_expect_tx(&bars->full[s], args.stage_bytes);
+                tma_load_3d(st, tm_w, &bars->full[s], n0, i * kSlab, 0);
+                tma_load_3d(st + kBoxBytes, tm_w, &bars->full[s], n0 + 64, i * kSlab, 0);
+                for (int j = 0; j < args.nb; ++j)
+                    tma_load_3d(st + 2 * kBoxBytes + j * kBoxBytes, &tm_x, &bars->full[s], i * kSlab, j * 64, 0);
+                loaded = i + 1;
+            }
+            // drain: every issued load has landed before the CTA can exit (bounded)
+            for (int i = (loaded > kGStages ? loaded - kGStages : 0); i < loaded; ++i)
+                (void)mbar_wait(&bars->full[i % kGStages], (i / kGStages) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // MMA issuer
+            int issued = 0;
+            for (int i = 0; i < n_slabs; ++i) {
+                const int s = i % kGStages;
+                if (!mbar_wait_or_abort(&bars->full[s], (i / kGStages) & 1, abort_flag)) break;
+                tc_fence_after();
+                const uint32_t st = sbase + s * args.stage_bytes;
+#pragma unroll
+                for (int kk = 0; kk < kSlab / 16; ++kk)
+                    mma_bf16(tmem, make_sdesc(st + kk * 2048, kBoxBytes, 1024),
+                             make_sdesc(st + 2 * kBoxBytes + kk * 32, 16, 1024), args.idesc, (i > 0 || kk > 0));
+                mma_commit(&bars->empty[s]);
+                issued = i + 1;
+            }
+            if (issued == n_slabs) {
+                mma_commit(&bars->done);
+            } else if (issued > 0) {  // drain what was issued (bounded)
+                (void)mbar_wait(&bars->empty[(issued - 1) % kGStages], ((issued - 1) / kGStages) & 1);
+            }
+        }
+    } else {  // epilogue: warps 2..5 cover the four lane quadrants
+        const int quad = warp & 3;
+        const int n = n0 + quad * 32 + lane;
+        const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        const bool ok = mbar_wait_or_abort(&bars->done, 0, abort_flag);
+        tc_fence_after();
+        if (ok) {
+            __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out[g]);
+            const int N = args.N[g];
+#pragma unroll 1
+            for (int b0 = 0; b0 < args.npad; b0 += 32) {
+                float x[32];
+                tmem_ld32(trow + b0, x);
+                tmem_wait_ld();
+                if (n < N) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (b0 + j < args.B) out[(size_t)(b0 + j) * N + n] = __float2bfloat16_rn(x[j]);
+                }
+            }
+        }
+    }
+    __syncwarp();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && bars->abort) atomicExch(args.status, (int32_t)GDN_ERR_TIMEOUT);
+    if (warp == 1) tmem_dealloc(tmem, args.tmem_cols);
+}
+
+// ------------------------------------------------------------------ host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// A [rows][cols] bf16 matrix (cols contiguous) as a 3-D map with a unit last
+// dimension, boxes of 64 x 64 with the 128-byte swizzle; out-of-range rows and
+// columns of a box read as zero.
+bool encode_2d(CUtensorMap* map, const void* ptr, long long rows, long long cols) {
+    EncodeTiledFn enc = encoder();
+    if (!enc) return false;
+    cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, 1};
+    cuuint64_t strides[2] = {(cuuint64_t)cols * 2, (cuuint64_t)rows * cols * 2};
+    cuuint32_t box[3] = {64, 64, 1}, estr[3] = {1, 1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct BlockLayout {
+    long long C, VD;           // conv_dim, value_dim
+    size_t off_raw, off_conv, off_z, off_a, off_b, bytes;
+};
+
+BlockLayout layout(const gdn_block_dims* d) {
+    BlockLayout L;
+    L.C = 2 * d->Hk * d->Dk + d->Hv * d->Dv;
+    L.VD = d->Hv * d->Dv;
+    auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
+    size_t o = 0;
+    L.off_raw = o;  o = up(o + (size_t)d->B * L.C * 2);
+    L.off_conv = o; o = up(o + (size_t)d->B * L.C * 2);
+    L.off_z = o;    o = up(o + (size_t)d->B * L.VD * 2);
+    L.off_a = o;    o = up(o + (size_t)d->B * d->Hv * 2);
+    L.off_b = o;    o = up(o + (size_t)d->B * d->Hv * 2);
+    L.bytes = o;
+    return L;
+}
+
+gdn_status check_block(const gdn_block_dims* d) {
+    if (!d) return GDN_ERR_NULL;
+    if (d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;  // bf16 weights and activations (Parameters)
+    if (d->flags != 0) return GDN_ERR_UNSUPPORTED;
+    if (d->B < 0 || d->H < 1 || d->Hk < 1 || d->Hv < 1 || d->Dk < 1 || d->Dv < 1 || d->K < 1) return GDN_ERR_DIMS;
+    if (d->Dk > 128 || d->Dv > 128 || d->Hv % d->Hk != 0) return GDN_ERR_DIMS;
+    if (d->K > 8 || d->B > 256 || d->H % 64 != 0) return GDN_ERR_UNSUPPORTED;
+    const long long C = 2 * d->Hk * d->Dk + d->Hv * d->Dv;
+    // TMA row pitches are multiples of 16 bytes
+    if (C % 8 != 0 || (d->Hv * d->Dv) % 8 != 0 || d->Hv % 8 != 0) return GDN_ERR_UNSUPPORTED;
+    if (C > INT32_MAX || d->B * C > INT32_MAX) return GDN_ERR_DIMS;
+    return GDN_OK;
+}
+
+}  // namespace
+}  // namespace gdn
+
+using namespace gdn;
+
+extern "C" size_t gdn_decode_block_workspace_bytes(const gdn_block_dims* dims) {
+    if (check_block(dims) != GDN_OK) return 0;
+    return layout(dims).bytes;
+}
+
+extern "C" gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, const void* W_z, const void* W_a,
+                                       const void* W_b, const float* conv_weight, void* conv_state_inout,
+                                       const float* A_log, const float* dt_bias, const float* norm_weight,
+                                       float* state_inout, void* out, void* workspace, size_t workspace_bytes,
+                                       const gdn_block_dims* d, gdn_stream_t stream) {
+    gdn_status st = check_block(d);
+    if (st != GDN_OK || d->B == 0) return st;
+    if (!hidden || !W_qkv || !W_z || !W_a || !W_b || !conv_weight || !conv_state_inout || !A_log || !dt_bias ||
+        !norm_weight || !state_inout || !out || !workspace)
+        return GDN_ERR_NULL;
+    const void* aligned_ptrs[] = {hidden, W_qkv, W_z, W_a, W_b, workspace};
+    for (const void* p : aligned_ptrs)
+        if (reinterpret_cast<uintptr_t>(p) & 15u) return GDN_ERR_ALIGN;
+    const BlockLayout L = layout(d);
+    if (workspace_bytes < L.bytes) return GDN_ERR_DIMS;
+    uint8_t* ws = static_cast<uint8_t*>(workspace);
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+
+    // 1. the four input projections
+    CUtensorMap tx, tw[kMaxGroups];
+    const void* W[kMaxGroups] = {W_qkv, W_z, W_a, W_b};
+    const long long N[kMaxGroups] = {L.C, L.VD, d->Hv, d->Hv};
+    void* outs[kMaxGroups] = {ws + L.off_raw, ws + L.off_z, ws + L.off_a, ws + L.off_b};
+    if (!encode_2d(&tx, hidden, d->B, d->H)) return GDN_ERR_CUDA;
+    GemmArgs a{};
+    int tiles = 0;
+    for (int g = 0; g < kMaxGroups; ++g) {
+        if (!encode_2d(&tw[g], W[g], d->H, N[g])) return GDN_ERR_CUDA;
+        a.out[g] = outs[g];
+        a.N[g] = (int)N[g];
+        a.tile_start[g] = tiles;
+        tiles += (int)((N[g] + kGTile - 1) / kGTile);
+    }
+    a.tile_start[kMaxGroups] = tiles;
+    a.B = (int)d->B;
+    a.H = (int)d->H;
+    a.nb = (int)((d->B + 63) / 64);
+    a.npad = (int)((d->B + 15) / 16 * 16);
+    a.stage_bytes = 2 * kBoxBytes + a.nb * kBoxBytes;
+    uint32_t cols = 32;
+    while (cols < (uint32_t)a.npad) cols <<= 1;
+    a.tmem_cols = cols;
+    a.idesc = make_idesc_bf16(128, a.npad, 1, 0);
+    if ((st = status_word_for_current_device(&a.status)) != GDN_OK) return st;
+    const size_t smem = kGStages * a.stage_bytes + sizeof(GemmBars) + 1024;
+    static std::once_flag attr_once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(attr_once, [] {
+        attr_err = cudaFuncSetAttribute(inproj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        kGStages * (2 + 4) * kBoxBytes + (int)sizeof(GemmBars) + 1024);
+    });
+    if (attr_err != cudaSuccess) return GDN_ERR_CUDA;
+    inproj_gemm_kernel<<<tiles, kGThreads, smem, s>>>(tx, tw[0], tw[1], tw[2], tw[3], a);
+    if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
+
+    // 2. conv1d decode on the q|k|v projection (a fresh window shift per call)
+    const gdn_conv_dims cd{d->B, L.C, 1, d->K, GDN_BF16, 0};
+    if ((st = gdn_conv1d_decode(ws + L.off_raw, conv_weight, conv_state_inout, ws + L.off_conv, &cd, stream)) !=
+        GDN_OK)
+        return st;
+
+    // 3. the gated step on the conv output
+    const gdn_dims gd{d->B, d->Hk, d->Hv, 1, d->Dk, d->Dv, GDN_BF16, 0};
+    return gdn_decode_gated(ws + L.off_conv, ws + L.off_z, ws + L.off_a, ws + L.off_b, A_log, dt_bias, norm_weight,
+                            1.0f / std::sqrt((float)d->Dk), state_inout, out, &gd, stream);
+}

@@ -11,7 +11,6 @@
 
 namespace gdn {
 namespace {
-
 // Kernel-side status word of each device (0 = fine, else a gdn_status).  Its
 // device address is looked up once per device, with that device current.
 __device__ int32_t g_status_word;
@@ -19,6 +18,8 @@ __device__ int32_t g_status_word;
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 int32_t* g_status_addr[kMaxDevices] = {};
+
+}  // namespace
 
 gdn_status status_word_for_current_device(int32_t** out) {
     int dev = 0;
@@ -32,6 +33,9 @@ gdn_status status_word_for_current_device(int32_t** out) {
     *out = g_status_addr[dev];
     return GDN_OK;
 }
+
+
+namespace {
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 

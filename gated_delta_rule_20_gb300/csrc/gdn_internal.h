@@ -23,6 +23,10 @@ struct Problem {
     bool zero_init;  // GDN_ZERO_INITIAL_STATE
 };
 
+// Device address of the current device's kernel-side status word (0 = fine,
+// else a gdn_status written by a kernel whose wait gave up).
+gdn_status status_word_for_current_device(int32_t** out);
+
 // Decode step (S == 1): one pass over the fp32 state.
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 

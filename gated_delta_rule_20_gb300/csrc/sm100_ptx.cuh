@@ -66,7 +66,7 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Wait for the phase with the given parity to complete; false after ~1 s.
 // The polling loops are out of line (one copy in the program) and only entered
 // when the first test fails, to keep the inlined code of each wait small.
-__device__ __noinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t parity) {
+static __device__ __noinline__ bool mbar_wait_loop(uint64_t* bar, uint32_t parity) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
@@ -81,7 +81,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // The thread polls (try_wait without a suspend hint blocks for a short,
 // hardware-chosen time per test): resuming from a suspended try_wait was
 // measured to cost more than the polling does.
-__device__ __noinline__ bool mbar_wait_or_abort_loop(uint64_t* bar, uint32_t parity, volatile int* abort) {
+static __device__ __noinline__ bool mbar_wait_or_abort_loop(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const uint64_t t0 = globaltimer_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;

@@ -200,6 +200,50 @@ gdn_status gdn_conv1d_prefill(const void* mixed, const float* conv_weight, void*
 gdn_status gdn_conv1d_decode(const void* x, const float* conv_weight, void* conv_state_inout, void* out,
                              const gdn_conv_dims* dims, gdn_stream_t stream);
 
+/*
+ * The decode block without its output projection ("GDN Block TKG Kernel API
+ * Reference": gdn_block_tkg Parameters, Returns, Notes; the data flow "in_proj
+ * matmuls -> gdn_conv1d_decode -> split conv_out + GQA-repeat q,k -> gdn_tkg"):
+ * the four input projections of one token's hidden state, the conv1d decode step
+ * on the q|k|v channels, and the gated single-token step (gdn_decode_gated, with
+ * the query scale 1/sqrt(Dk), the page having no scale argument).
+ *
+ *   B in [0, 256]; H (hidden size) a multiple of 64; Hk, Hv, Dk, Dv as for
+ *   gdn_decode_step; K in [1, 8] conv taps; dtype GDN_BF16 (the page's bf16
+ *   weights and activations; others return GDN_ERR_UNSUPPORTED); flags 0.
+ *   conv_dim C = 2*Hk*Dk + Hv*Dv; value_dim = Hv*Dv; C, value_dim and Hv must be
+ *   multiples of 8 (row pitches of 16 bytes).
+ */
+typedef struct {
+    int64_t B, H, Hk, Hv, Dk, Dv, K;
+    int32_t dtype;   /* GDN_BF16 */
+    uint32_t flags;  /* 0 */
+} gdn_block_dims;
+
+/* Device workspace bytes gdn_decode_block needs (the inter-stage activations:
+ * the q|k|v projection and its conv output, z, a, b in bf16); 0 for invalid dims. */
+size_t gdn_decode_block_workspace_bytes(const gdn_block_dims* dims);
+
+/*
+ * gdn_decode_block -- one token through the block.
+ *   hidden            [B, 1, H] bf16
+ *   W_qkv             [H, C] bf16, W_z [H, value_dim] bf16, W_a, W_b [H, Hv] bf16
+ *                     (each == nn.Linear.weight.T)
+ *   conv_weight       [C, K] fp32;  conv_state_inout [B, C, K] bf16, shifted in place
+ *   A_log, dt_bias    [Hv] fp32;    norm_weight [Dv] fp32
+ *   state_inout       [B, Hv, Dk, Dv] fp32, updated in place
+ *   out               [B, 1, value_dim] bf16, the RMSNormGated output
+ *   workspace         device memory of at least gdn_decode_block_workspace_bytes,
+ *                     16-byte aligned, owned by the caller (else GDN_ERR_DIMS)
+ * hidden, the weights and the workspace must be 16-byte aligned (GDN_ERR_ALIGN).
+ * Launches three kernels on `stream`.
+ */
+gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, const void* W_z, const void* W_a,
+                            const void* W_b, const float* conv_weight, void* conv_state_inout,
+                            const float* A_log, const float* dt_bias, const float* norm_weight,
+                            float* state_inout, void* out, void* workspace, size_t workspace_bytes,
+                            const gdn_block_dims* dims, gdn_stream_t stream);
+
 /* Device workspace gdn_prefill needs for these dims: always 0 (every kernel
  * keeps its intermediates on chip). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);
@@ -215,7 +259,8 @@ const char* gdn_status_string(gdn_status s);
  */
 gdn_status gdn_device_status(int device, int clear, int32_t* code);
 
-/* Number of kernels one call launches (every entry point launches at most one). */
+/* Number of kernels one call of gdn_prefill, gdn_decode_step, gdn_decode_gated or
+ * the conv1d entry points launches (one); gdn_decode_block launches three. */
 int gdn_kernels_per_call(void);
 
 #ifdef __cplusplus

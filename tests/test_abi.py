@@ -145,3 +145,26 @@ def test_decode_gated_argument_checks(L):
     assert call(D(), st=None) == gdn.GDN_ERR_NULL
     assert call(D(), a=ctypes.c_void_p(0x1001)) == gdn.GDN_ERR_ALIGN
     assert call(D(B=0)) == gdn.GDN_OK
+
+
+def test_decode_block_argument_checks(L):
+    """Host-side checks of gdn_decode_block and its workspace query (no GPU needed)."""
+    p = ctypes.c_void_p(0x1000)
+    D = lambda **kw: gdn.GdnBlockDims(kw.get("B", 2), kw.get("H", 128), kw.get("Hk", 2), kw.get("Hv", 8),
+                                      kw.get("Dk", 64), kw.get("Dv", 64), kw.get("K", 4),
+                                      kw.get("dtype", gdn.GDN_BF16), kw.get("flags", 0))
+    call = lambda d, ws=1 << 30, hid=p: L.gdn_decode_block(hid, p, p, p, p, p, p, p, p, p, p, p, p, ctypes.c_size_t(ws),
+                                                          ctypes.byref(d) if d is not None else None, None)
+    assert call(None) == gdn.GDN_ERR_NULL
+    assert call(D(dtype=gdn.GDN_F32)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(D(H=100)) == gdn.GDN_ERR_UNSUPPORTED       # H % 64
+    assert call(D(B=300)) == gdn.GDN_ERR_UNSUPPORTED       # B > 256
+    assert call(D(K=9)) == gdn.GDN_ERR_UNSUPPORTED
+    assert call(D(Hv=4)) == gdn.GDN_ERR_UNSUPPORTED        # Hv % 8 (16-byte rows of W_a, W_b)
+    assert call(D(Dk=129)) == gdn.GDN_ERR_DIMS
+    assert call(D(), ws=16) == gdn.GDN_ERR_DIMS            # workspace too small
+    assert call(D(), hid=ctypes.c_void_p(0x1008)) == gdn.GDN_ERR_ALIGN
+    assert call(D(B=0)) == gdn.GDN_OK
+    need = L.gdn_decode_block_workspace_bytes(ctypes.byref(D(B=64, H=2048, Hk=16, Hv=32, Dk=128, Dv=128)))
+    assert need >= 64 * (2 * 8192 + 4096 + 64) * 2
+    assert L.gdn_decode_block_workspace_bytes(ctypes.byref(D(dtype=gdn.GDN_F32))) == 0
