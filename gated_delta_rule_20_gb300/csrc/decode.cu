@@ -92,6 +92,9 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_decode_kernel(const T* __rest
         S[i] = x;
     }
 
+    // the value row is fetched now too, so that its load does not wait behind a barrier
+    const int cv = c_base + (tid & (kCols - 1));
+    const float vc = (tid < kCols && cv < Dv) ? to_f32(v[(size_t)bh * Dv + cv]) : 0.f;
     if (tid < Dk) {
         s_k[tid] = to_f32(kp[tid]);
         s_q[tid] = to_f32(qp[tid]);
@@ -132,7 +135,6 @@ __global__ void __launch_bounds__(kThreads, 4) gdn_decode_kernel(const T* __rest
             sq += s_red[1][g][tid];
         }
         const int c = c_base + tid;
-        const float vc = (c < Dv) ? to_f32(v[(size_t)bh * Dv + c]) : 0.f;
         const float d = bt * (vc - a * sk);
         s_d[tid] = d;
         if (c < Dv) out[(size_t)bh * Dv + c] = from_f32<T>(scale * (a * sq + d * s_kq));

@@ -76,11 +76,11 @@ struct GatedArgs {
 
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs p) {
-    __shared__ float s_k[128], s_q[128];
+    __shared__ float s_k[128], s_q[128];  // raw q and k; their norms are applied to the reductions
     __shared__ float s_red[2][kRowGroups][128];
     __shared__ float s_d[128];
-    __shared__ float s_part[3][8];  // per-warp partial sums
-    __shared__ float s_scalar[4];   // |q|^2, |k|^2, k.q, sum o^2
+    __shared__ float s_v[128], s_gate[128];  // v, and norm_weight * silu(z)
+    __shared__ float s_part[4][kThreads / 32];  // per-warp partial sums: |q|^2, |k|^2, k.q, sum o^2
 
     const int bh = blockIdx.x;
     const int Hv = p.Hv, Dk = p.Dk, Dv = p.Dv;
@@ -116,11 +116,23 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
         S[i] = x;
     }
 
-    // prologue: q, k and their norms; the gates
+    // every other input of the head is fetched now too, so that no load waits behind a barrier
     float qv = 0.f, kv = 0.f;
     if (tid < Dk) {
         qv = to_f32(qp[tid]);
         kv = to_f32(kp[tid]);
+    }
+    if (tid < Dv) {
+        const float zv = to_f32(static_cast<const T*>(p.z)[(long long)bh * Dv + tid]);
+        s_v[tid] = to_f32(vp[tid]);
+        s_gate[tid] = p.norm_weight[tid] * (zv / (1.f + expf(-zv)));
+    }
+    const float a_in = to_f32(static_cast<const T*>(p.a)[bh]), b_in = to_f32(static_cast<const T*>(p.b)[bh]);
+    const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
+
+    if (tid < Dk) {
+        s_q[tid] = qv;
+        s_k[tid] = kv;
     }
     {
         const float sq = warp_sum(qv * qv), sk = warp_sum(kv * kv), skq = warp_sum(qv * kv);
@@ -130,26 +142,21 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
             s_part[2][warp] = skq;
         }
     }
-    __syncthreads();
-    if (tid < 3) {
-        float t = 0.f;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) t += s_part[tid][w];
-        s_scalar[tid] = t;
-    }
-    __syncthreads();
-    const float inv_q = rsqrtf(s_scalar[0] + kEpsL2), inv_k = rsqrtf(s_scalar[1] + kEpsL2);
-    const float kq = s_scalar[2] * inv_q * inv_k;
-    if (tid < Dk) {
-        s_q[tid] = qv * inv_q;
-        s_k[tid] = kv * inv_k;
-    }
-    const float g = -expf(p.A_log[h]) * softplus(to_f32(static_cast<const T*>(p.a)[bh]) + p.dt_bias[h]);
+    const float g = -expf(A_log) * softplus(a_in + dt_bias);
     const float decay = expf(g);
-    const float beta = 1.f / (1.f + expf(-to_f32(static_cast<const T*>(p.b)[bh])));
+    const float beta = 1.f / (1.f + expf(-b_in));
     __syncthreads();
+    float nq = 0.f, nk = 0.f, nkq = 0.f;
+#pragma unroll
+    for (int w = 0; w < kThreads / 32; ++w) {
+        nq += s_part[0][w];
+        nk += s_part[1][w];
+        nkq += s_part[2][w];
+    }
+    const float inv_q = rsqrtf(nq + kEpsL2), inv_k = rsqrtf(nk + kEpsL2);
+    const float kq = nkq * inv_q * inv_k;
 
-    // S^T k^ and S^T q^: partials over this thread's rows, then over the row groups
+    // S^T k and S^T q with the raw vectors: partials over this thread's rows, then over the row groups
     float pk[4] = {0.f, 0.f, 0.f, 0.f}, pq[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int i = 0; i < kMaxRows; ++i) {
@@ -180,37 +187,23 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
             sk += s_red[0][gi][tid];
             sq += s_red[1][gi][tid];
         }
-        const float d = beta * (to_f32(vp[tid]) - decay * sk);
+        const float d = beta * (s_v[tid] - decay * (sk * inv_k));
         s_d[tid] = d;
-        o = p.scale * (decay * sq + d * kq);
+        o = p.scale * (decay * (sq * inv_q) + d * kq);
     }
-    // epilogue: RMS of o over the head, gate, store
     {
         const float so = warp_sum(o * o);
-        if (lane == 0) s_part[0][warp] = so;
+        if (lane == 0) s_part[3][warp] = so;
     }
     __syncthreads();
-    if (tid == 0) {
-        float t = 0.f;
-#pragma unroll
-        for (int w = 0; w < kThreads / 32; ++w) t += s_part[0][w];
-        s_scalar[3] = t;
-    }
-    __syncthreads();
-    if (tid < Dv) {
-        const float rinv = rsqrtf(s_scalar[3] / (float)Dv + kEpsRms);
-        const float zv = to_f32(static_cast<const T*>(p.z)[(long long)bh * Dv + tid]);
-        const float gate = zv / (1.f + expf(-zv));
-        static_cast<T*>(p.out)[(long long)bh * Dv + tid] = from_f32<T>(o * rinv * p.norm_weight[tid] * gate);
-    }
 
-    // S' = e^g S + k^ d^T, in place
+    // S' = e^g S + k^ d^T, in place; the stores go out before the output epilogue
     const float d0 = s_d[c0 + 0], d1 = s_d[c0 + 1], d2 = s_d[c0 + 2], d3 = s_d[c0 + 3];
 #pragma unroll
     for (int i = 0; i < kMaxRows; ++i) {
         const int r = rg + i * kRowGroups;
         if (r < Dk) {
-            const float kr = s_k[r];
+            const float kr = s_k[r] * inv_k;
             float4 x;
             x.x = fmaf(decay, S[i].x, kr * d0);
             x.y = fmaf(decay, S[i].y, kr * d1);
@@ -226,6 +219,15 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
                 if (c0 + 3 < Dv) row[c0 + 3] = x.w;
             }
         }
+    }
+
+    // epilogue: RMS of o over the head, gate, store
+    if (tid < Dv) {
+        float so = 0.f;
+#pragma unroll
+        for (int w = 0; w < kThreads / 32; ++w) so += s_part[3][w];
+        const float rinv = rsqrtf(so / (float)Dv + kEpsRms);
+        static_cast<T*>(p.out)[(long long)bh * Dv + tid] = from_f32<T>(o * rinv * s_gate[tid]);
     }
 }
 
