@@ -1,21 +1,32 @@
 // block.cu -- the decode block without its output projection ("GDN Block TKG
 // Kernel API Reference": gdn_block_tkg Parameters, Returns, Notes and the data
 // flow "in_proj matmuls -> gdn_conv1d_decode -> split conv_out + GQA-repeat q,k
-// -> gdn_tkg").  Three launches on the caller's stream:
+// -> gdn_tkg").  Two launches on the caller's stream:
 //
 //   1. the four input projections of the token's hidden state, one grouped
 //      tcgen05 GEMM (this file): [B, H] x [H, N] for N = conv_dim, value_dim,
-//      num_v_heads, num_v_heads, written to the caller's workspace in bf16;
-//   2. gdn_conv1d_decode on the q|k|v projection (conv1d.cu);
-//   3. gdn_decode_gated on the conv output, z, a and b (decode_gated.cu).
+//      num_v_heads, num_v_heads.  z, a and b go to the caller's workspace in
+//      bf16.  The q|k|v projection is not written out: the thread that holds
+//      its output column n holds channel n for every token, so it shifts that
+//      channel's conv window in place, appending the new value (rounded to
+//      bf16) -- the window then holds everything the conv1d decode step needs;
+//   2. the gated step (decode_gated.cu) in its conv mode: each q, k, v value is
+//      silu(sum_k w[c, k] window[b, c, k]), rounded to bf16, computed where it
+//      is consumed -- the arithmetic, tap order and roundings of
+//      gdn_conv1d_decode.  It is launched as a programmatic dependent of the
+//      GEMM: its CTAs start once every GEMM CTA is resident, load their fp32
+//      state while the GEMM runs, and wait for it before reading its outputs.
 //
 // The GEMM is a weight stream (M = B tokens is small): each CTA owns 128 output
 // columns of one weight matrix and runs over H in 64-row slabs.  The product is
 // issued transposed, D^T[n][b] = sum_h W[h][n] X[b][h], so the 128 columns sit on
 // the tcgen05 M / TMEM-lane axis and the batch on N: A = the W slab (MN-major,
 // two 64-column boxes with the 128-byte swizzle), B = the hidden rows (K-major).
-// Warp 0 issues the TMA loads through kGStages stages, warp 1 the MMAs, warps
+// Warp 0 issues the TMA loads through args.stages stages, warp 1 the MMAs, warps
 // 2..5 write the fp32 accumulator back as bf16 (one TMEM lane quadrant each).
+// While the main loop runs, the epilogue warps of the q|k|v CTAs copy their conv
+// windows (B <= 64) to shared memory with cp.async.  The pipeline is as deep as
+// 200 KB of shared memory allows, which leaves room for a CTA of the gated step.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -33,38 +44,46 @@ using namespace ptx;
 
 constexpr int kGTile = 128;   // output columns per CTA
 constexpr int kSlab = 64;     // hidden rows per stage
-constexpr int kGStages = 4;
+constexpr int kMaxStages = 8;
+constexpr int kSmemBudget = 200 * 1024;   // leaves room for a CTA of the gated step on the same SM
+constexpr int kWinTokens = 64;            // conv windows staged in shared memory up to this batch
 constexpr int kGThreads = 192;
 constexpr uint32_t kBoxBytes = 64 * 128;  // [64 rows][64 bf16]
 constexpr int kMaxGroups = 4;
 
 struct GemmArgs {
-    void* out[kMaxGroups];        // [B][N_g] bf16
+    void* out[kMaxGroups];        // [B][N_g] bf16 (group 0: none, its values go to the windows)
     int N[kMaxGroups];
+    __nv_bfloat16* conv_state;    // [B][N_0][K]: group 0's conv windows, shifted in place
+    int K, conv_vec4;             // conv_vec4: K == 4 with 8-byte windows
     int tile_start[kMaxGroups + 1];
     int B, H, nb, npad;           // nb = hidden boxes of 64 rows; npad = MMA N
+    int stages;                   // pipeline depth, <= kMaxStages
     uint32_t stage_bytes, tmem_cols, idesc;
+    uint32_t win_off, win_bytes;  // staged conv windows [B][kGTile] uint2 (0 bytes: read from global)
     int32_t* status;
 };
 
 struct GemmBars {
-    uint64_t full[kGStages];
-    uint64_t empty[kGStages];
+    uint64_t full[kMaxStages];
+    uint64_t empty[kMaxStages];
     uint64_t done;
     uint32_t tmem_base;
     int abort;
 };
 
-__global__ void __launch_bounds__(kGThreads, 1)
+__global__ void __launch_bounds__(kGThreads, 2)
     inproj_gemm_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w0,
                        const __grid_constant__ CUtensorMap tm_w1, const __grid_constant__ CUtensorMap tm_w2,
-                       const __grid_constant__ CUtensorMap tm_w3, const GemmArgs args) {
+                       const __grid_constant__ CUtensorMap tm_w3, const __grid_constant__ GemmArgs args) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sbase = smem_u32(sm);
-    GemmBars* bars = reinterpret_cast<GemmBars*>(sm + kGStages * args.stage_bytes);
+    const int stages = args.stages;
+    GemmBars* bars = reinterpret_cast<GemmBars*>(sm + stages * args.stage_bytes);
     volatile int* abort_flag = &bars->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    ptx::griddep_launch_dependents();  // the gated step may start its state loads now
 
     int g = 0;  // weight matrix of this CTA
     while (g + 1 < kMaxGroups && (int)blockIdx.x >= args.tile_start[g + 1]) ++g;
@@ -73,7 +92,7 @@ __global__ void __launch_bounds__(kGThreads, 1)
     const int n_slabs = args.H / kSlab;
 
     if (tid == 0) {
-        for (int s = 0; s < kGStages; ++s) {
+        for (int s = 0; s < stages; ++s) {
             mbar_init(&bars->full[s], 1);
             mbar_init(&bars->empty[s], 1);
         }
@@ -96,8 +115,8 @@ __global__ void __launch_bounds__(kGThreads, 1)
             tma_prefetch_desc(tm_w);
             int loaded = 0;
             for (int i = 0; i < n_slabs; ++i) {
-                const int s = i % kGStages;
-                if (i >= kGStages && !mbar_wait_or_abort(&bars->empty[s], ((i / kGStages) - 1) & 1, abort_flag)) break;
+                const int s = i % stages;
+                if (i >= stages && !mbar_wait_or_abort(&bars->empty[s], ((i / stages) - 1) & 1, abort_flag)) break;
                 uint8_t* st = sm + s * args.stage_bytes;
                 mbar_arrive_expect_tx(&bars->full[s], args.stage_bytes);
                 tma_load_3d(st, tm_w, &bars->full[s], n0, i * kSlab, 0);
@@ -107,15 +126,15 @@ __global__ void __launch_bounds__(kGThreads, 1)
                 loaded = i + 1;
             }
             // drain: every issued load has landed before the CTA can exit (bounded)
-            for (int i = (loaded > kGStages ? loaded - kGStages : 0); i < loaded; ++i)
-                (void)mbar_wait(&bars->full[i % kGStages], (i / kGStages) & 1);
+            for (int i = (loaded > stages ? loaded - stages : 0); i < loaded; ++i)
+                (void)mbar_wait(&bars->full[i % stages], (i / stages) & 1);
         }
     } else if (warp == 1) {
         if (lane == 0) {  // MMA issuer
             int issued = 0;
             for (int i = 0; i < n_slabs; ++i) {
-                const int s = i % kGStages;
-                if (!mbar_wait_or_abort(&bars->full[s], (i / kGStages) & 1, abort_flag)) break;
+                const int s = i % stages;
+                if (!mbar_wait_or_abort(&bars->full[s], (i / stages) & 1, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t st = sbase + s * args.stage_bytes;
 #pragma unroll
@@ -128,27 +147,70 @@ __global__ void __launch_bounds__(kGThreads, 1)
             if (issued == n_slabs) {
                 mma_commit(&bars->done);
             } else if (issued > 0) {  // drain what was issued (bounded)
-                (void)mbar_wait(&bars->empty[(issued - 1) % kGStages], ((issued - 1) / kGStages) & 1);
+                (void)mbar_wait(&bars->empty[(issued - 1) % stages], ((issued - 1) / stages) & 1);
             }
         }
     } else {  // epilogue: warps 2..5 cover the four lane quadrants
         const int quad = warp & 3;
         const int n = n0 + quad * 32 + lane;
         const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        const int N = args.N[g];
+        const bool conv = g == 0;
+        // while the main loop runs, this thread's conv windows (channel n, every token) are
+        // copied to shared memory, so that the epilogue does not wait on them
+        uint2* win = reinterpret_cast<uint2*>(sm + args.win_off) + quad * 32 + lane;
+        const bool staged = conv && args.win_bytes != 0 && n < N;
+        if (staged) {
+            const uint2* src = reinterpret_cast<const uint2*>(args.conv_state) + n;
+            for (int b = 0; b < args.B; ++b) cp_async_8(win + b * kGTile, src + (size_t)b * N);
+            cp_async_commit();
+        }
         const bool ok = mbar_wait_or_abort(&bars->done, 0, abort_flag);
         tc_fence_after();
+        if (staged) cp_async_wait_all();
         if (ok) {
             __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out[g]);
-            const int N = args.N[g];
 #pragma unroll 1
             for (int b0 = 0; b0 < args.npad; b0 += 32) {
                 float x[32];
                 tmem_ld32(trow + b0, x);
                 tmem_wait_ld();
-                if (n < N) {
+                if (n >= N) continue;
+                if (!conv) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
                         if (b0 + j < args.B) out[(size_t)(b0 + j) * N + n] = __float2bfloat16_rn(x[j]);
+                } else if (args.conv_vec4) {
+                    // window = 4 bf16 (oldest first) in one 8-byte word: drop the oldest, append x
+                    uint2* sp = reinterpret_cast<uint2*>(args.conv_state) + (size_t)b0 * N + n;
+#pragma unroll
+                    for (int h = 0; h < 32; h += 16) {
+                        uint2 sv[16];
+                        if (staged) {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                sv[j] = (b0 + h + j < args.B) ? win[(b0 + h + j) * kGTile] : make_uint2(0u, 0u);
+                        } else {
+#pragma unroll
+                            for (int j = 0; j < 16; ++j)
+                                sv[j] = (b0 + h + j < args.B) ? sp[(size_t)(h + j) * N] : make_uint2(0u, 0u);
+                        }
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            if (b0 + h + j >= args.B) continue;
+                            const uint32_t xb = __bfloat16_as_ushort(__float2bfloat16_rn(x[h + j]));
+                            sp[(size_t)(h + j) * N] =
+                                make_uint2((sv[j].x >> 16) | (sv[j].y << 16), (sv[j].y >> 16) | (xb << 16));
+                        }
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        if (b0 + j >= args.B) continue;
+                        __nv_bfloat16* sp = args.conv_state + ((size_t)(b0 + j) * N + n) * args.K;
+                        for (int k = 0; k + 1 < args.K; ++k) sp[k] = sp[k + 1];
+                        sp[args.K - 1] = __float2bfloat16_rn(x[j]);
+                    }
                 }
             }
         }
@@ -195,7 +257,7 @@ bool encode_2d(CUtensorMap* map, const void* ptr, long long rows, long long cols
 
 struct BlockLayout {
     long long C, VD;           // conv_dim, value_dim
-    size_t off_raw, off_conv, off_z, off_a, off_b, bytes;
+    size_t off_z, off_a, off_b, bytes;
 };
 
 BlockLayout layout(const gdn_block_dims* d) {
@@ -204,8 +266,6 @@ BlockLayout layout(const gdn_block_dims* d) {
     L.VD = d->Hv * d->Dv;
     auto up = [](size_t x) { return (x + 255) & ~(size_t)255; };
     size_t o = 0;
-    L.off_raw = o;  o = up(o + (size_t)d->B * L.C * 2);
-    L.off_conv = o; o = up(o + (size_t)d->B * L.C * 2);
     L.off_z = o;    o = up(o + (size_t)d->B * L.VD * 2);
     L.off_a = o;    o = up(o + (size_t)d->B * d->Hv * 2);
     L.off_b = o;    o = up(o + (size_t)d->B * d->Hv * 2);
@@ -250,6 +310,12 @@ extern "C" gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, co
     const void* aligned_ptrs[] = {hidden, W_qkv, W_z, W_a, W_b, workspace};
     for (const void* p : aligned_ptrs)
         if (reinterpret_cast<uintptr_t>(p) & 15u) return GDN_ERR_ALIGN;
+    // element alignment of the rest, checked before the first launch
+    if ((reinterpret_cast<uintptr_t>(conv_state_inout) | reinterpret_cast<uintptr_t>(out)) & 1u) return GDN_ERR_ALIGN;
+    if ((reinterpret_cast<uintptr_t>(conv_weight) | reinterpret_cast<uintptr_t>(A_log) |
+         reinterpret_cast<uintptr_t>(dt_bias) | reinterpret_cast<uintptr_t>(norm_weight) |
+         reinterpret_cast<uintptr_t>(state_inout)) & 3u)
+        return GDN_ERR_ALIGN;
     const BlockLayout L = layout(d);
     if (workspace_bytes < L.bytes) return GDN_ERR_DIMS;
     uint8_t* ws = static_cast<uint8_t*>(workspace);
@@ -259,7 +325,7 @@ extern "C" gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, co
     CUtensorMap tx, tw[kMaxGroups];
     const void* W[kMaxGroups] = {W_qkv, W_z, W_a, W_b};
     const long long N[kMaxGroups] = {L.C, L.VD, d->Hv, d->Hv};
-    void* outs[kMaxGroups] = {ws + L.off_raw, ws + L.off_z, ws + L.off_a, ws + L.off_b};
+    void* outs[kMaxGroups] = {nullptr, ws + L.off_z, ws + L.off_a, ws + L.off_b};
     if (!encode_2d(&tx, hidden, d->B, d->H)) return GDN_ERR_CUDA;
     GemmArgs a{};
     int tiles = 0;
@@ -271,35 +337,40 @@ extern "C" gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, co
         tiles += (int)((N[g] + kGTile - 1) / kGTile);
     }
     a.tile_start[kMaxGroups] = tiles;
+    a.conv_state = static_cast<__nv_bfloat16*>(conv_state_inout);
+    a.K = (int)d->K;
+    a.conv_vec4 = d->K == 4 && (reinterpret_cast<uintptr_t>(conv_state_inout) & 7u) == 0;
     a.B = (int)d->B;
     a.H = (int)d->H;
     a.nb = (int)((d->B + 63) / 64);
     a.npad = (int)((d->B + 15) / 16 * 16);
     a.stage_bytes = 2 * kBoxBytes + a.nb * kBoxBytes;
+    a.win_bytes = (a.B <= kWinTokens && a.conv_vec4) ? (uint32_t)(a.B * kGTile * 8) : 0u;
+    {
+        const int fixed = (int)((sizeof(GemmBars) + 15) & ~(size_t)15) + (int)a.win_bytes + 1024;
+        a.stages = (kSmemBudget - fixed) / (int)a.stage_bytes;
+        if (a.stages > kMaxStages) a.stages = kMaxStages;
+    }
+    a.win_off = (uint32_t)(a.stages * a.stage_bytes + ((sizeof(GemmBars) + 15) & ~(size_t)15));
     uint32_t cols = 32;
     while (cols < (uint32_t)a.npad) cols <<= 1;
     a.tmem_cols = cols;
     a.idesc = make_idesc_bf16(128, a.npad, 1, 0);
     if ((st = status_word_for_current_device(&a.status)) != GDN_OK) return st;
-    const size_t smem = kGStages * a.stage_bytes + sizeof(GemmBars) + 1024;
+    const size_t smem = a.win_off + a.win_bytes + 1024;
     static std::once_flag attr_once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(attr_once, [] {
         attr_err = cudaFuncSetAttribute(inproj_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        kGStages * (2 + 4) * kBoxBytes + (int)sizeof(GemmBars) + 1024);
+                                        kSmemBudget);
     });
     if (attr_err != cudaSuccess) return GDN_ERR_CUDA;
     inproj_gemm_kernel<<<tiles, kGThreads, smem, s>>>(tx, tw[0], tw[1], tw[2], tw[3], a);
     if (cudaGetLastError() != cudaSuccess) return GDN_ERR_CUDA;
 
-    // 2. conv1d decode on the q|k|v projection (a fresh window shift per call)
-    const gdn_conv_dims cd{d->B, L.C, 1, d->K, GDN_BF16, 0};
-    if ((st = gdn_conv1d_decode(ws + L.off_raw, conv_weight, conv_state_inout, ws + L.off_conv, &cd, stream)) !=
-        GDN_OK)
-        return st;
-
-    // 3. the gated step on the conv output
+    // 2. the conv output and the gated step, behind the GEMM
     const gdn_dims gd{d->B, d->Hk, d->Hv, 1, d->Dk, d->Dv, GDN_BF16, 0};
-    return gdn_decode_gated(ws + L.off_conv, ws + L.off_z, ws + L.off_a, ws + L.off_b, A_log, dt_bias, norm_weight,
-                            1.0f / std::sqrt((float)d->Dk), state_inout, out, &gd, stream);
+    const GatedConvInput conv{conv_state_inout, conv_weight, (int)d->K};
+    return decode_gated_checked(nullptr, ws + L.off_z, ws + L.off_a, ws + L.off_b, A_log, dt_bias, norm_weight,
+                                1.0f / std::sqrt((float)d->Dk), state_inout, out, &gd, s, true, &conv);
 }

@@ -20,7 +20,8 @@
 
 #include <cstdint>
 
-#include "gdn.h"
+#include "gdn_internal.h"
+#include "sm100_ptx.cuh"
 
 namespace gdn {
 namespace {
@@ -72,9 +73,41 @@ struct GatedArgs {
     float* state;
     void* out;
     int Hk, Hv, Dk, Dv, zero_init;
+    // conv mode: q|k|v come from the shifted conv windows [B, conv_dim, K] (bf16) and the
+    // taps [conv_dim, K] fp32, conv_out = silu(sum_k w[c, k] window[b, c, k]) rounded to bf16
+    const void* conv_win;
+    const float* conv_w;
+    int K;
 };
 
-template <typename T, bool kVec>
+// How the kernel gets q, k and v: kDirect reads them; kConv4 / kConvAny compute the
+// conv1d decode output from the window (K == 4 as one 8-byte word / any K).
+enum InputMode { kDirect = 0, kConv4 = 1, kConvAny = 2 };
+
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+
+template <typename T, int kMode>
+__device__ __forceinline__ float input_value(const GatedArgs& p, const T* row_in, long long row, long long ch) {
+    if constexpr (kMode == kDirect) {
+        return to_f32(row_in[ch]);
+    } else if constexpr (kMode == kConv4) {
+        const uint2 s = reinterpret_cast<const uint2*>(p.conv_win)[row + ch];
+        const float4 w = reinterpret_cast<const float4*>(p.conv_w)[ch];
+        float z = fmaf(w.x, __uint_as_float(s.x << 16), 0.f);
+        z = fmaf(w.y, __uint_as_float(s.x & 0xffff0000u), z);
+        z = fmaf(w.z, __uint_as_float(s.y << 16), z);
+        z = fmaf(w.w, __uint_as_float(s.y & 0xffff0000u), z);
+        return __bfloat162float(__float2bfloat16_rn(silu_fast(z)));
+    } else {
+        const __nv_bfloat16* s = static_cast<const __nv_bfloat16*>(p.conv_win) + (row + ch) * p.K;
+        const float* w = p.conv_w + ch * p.K;
+        float z = 0.f;
+        for (int k = 0; k < p.K; ++k) z = fmaf(w[k], __bfloat162float(s[k]), z);
+        return __bfloat162float(__float2bfloat16_rn(silu_fast(z)));
+    }
+}
+
+template <typename T, bool kVec, int kMode>
 __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs p) {
     __shared__ float s_k[128], s_q[128];  // raw q and k; their norms are applied to the reductions
     __shared__ float s_red[2][kRowGroups][128];
@@ -90,10 +123,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
     const int cg = tid & (kColGroups - 1), rg = tid >> 5;
     const int c0 = cg * 4;
     const long long conv_dim = 2LL * p.Hk * Dk + (long long)Hv * Dv;
-    const T* row_in = static_cast<const T*>(p.qkv) + b * conv_dim;
-    const T* qp = row_in + (long long)hk * Dk;
-    const T* kp = row_in + (long long)p.Hk * Dk + (long long)hk * Dk;
-    const T* vp = row_in + 2LL * p.Hk * Dk + (long long)h * Dv;
+    const T* row_in = static_cast<const T*>(p.qkv) + b * conv_dim;  // kDirect
+    const long long row = (long long)b * conv_dim;                     // conv modes
+    const long long ch_q = (long long)hk * Dk, ch_k = (long long)p.Hk * Dk + ch_q;
+    const long long ch_v = 2LL * p.Hk * Dk + (long long)h * Dv;
     float* Sp = p.state + (long long)bh * Dk * Dv;
 
     // the state loads go out first: they are the bulk of the traffic
@@ -115,16 +148,19 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
         }
         S[i] = x;
     }
+    // Behind a programmatic launch the loads above overlap the producer of the
+    // inputs below (the decode block's projection kernel); the state is not its output.
+    ptx::griddep_wait();
 
     // every other input of the head is fetched now too, so that no load waits behind a barrier
     float qv = 0.f, kv = 0.f;
     if (tid < Dk) {
-        qv = to_f32(qp[tid]);
-        kv = to_f32(kp[tid]);
+        qv = input_value<T, kMode>(p, row_in, row, ch_q + tid);
+        kv = input_value<T, kMode>(p, row_in, row, ch_k + tid);
     }
     if (tid < Dv) {
         const float zv = to_f32(static_cast<const T*>(p.z)[(long long)bh * Dv + tid]);
-        s_v[tid] = to_f32(vp[tid]);
+        s_v[tid] = input_value<T, kMode>(p, row_in, row, ch_v + tid);
         s_gate[tid] = p.norm_weight[tid] * (zv / (1.f + expf(-zv)));
     }
     const float a_in = to_f32(static_cast<const T*>(p.a)[bh]), b_in = to_f32(static_cast<const T*>(p.b)[bh]);
@@ -231,25 +267,46 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
     }
 }
 
+template <typename T, bool kVec, int kMode>
+cudaError_t launch_one(const GatedArgs& a, int B, cudaStream_t s, bool after_producer) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(B * a.Hv));
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_producer ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gdn_decode_gated_kernel<T, kVec, kMode>, a);
+}
+
 template <typename T>
-cudaError_t launch_gated(const GatedArgs& a, int B, cudaStream_t s) {
+cudaError_t launch_gated(const GatedArgs& a, int B, cudaStream_t s, bool after_producer) {
     const bool vec = (a.Dv % 4) == 0 && (reinterpret_cast<uintptr_t>(a.state) & 15u) == 0;
-    if (vec)
-        gdn_decode_gated_kernel<T, true><<<B * a.Hv, kThreads, 0, s>>>(a);
-    else
-        gdn_decode_gated_kernel<T, false><<<B * a.Hv, kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    return vec ? launch_one<T, true, kDirect>(a, B, s, after_producer)
+               : launch_one<T, false, kDirect>(a, B, s, after_producer);
+}
+
+cudaError_t launch_gated_conv(const GatedArgs& a, int B, cudaStream_t s, bool after_producer) {
+    using T = __nv_bfloat16;
+    const bool vec = (a.Dv % 4) == 0 && (reinterpret_cast<uintptr_t>(a.state) & 15u) == 0;
+    const bool conv4 = a.K == 4 && (reinterpret_cast<uintptr_t>(a.conv_win) & 7u) == 0 &&
+                       (reinterpret_cast<uintptr_t>(a.conv_w) & 15u) == 0;
+    if (conv4)
+        return vec ? launch_one<T, true, kConv4>(a, B, s, after_producer)
+                   : launch_one<T, false, kConv4>(a, B, s, after_producer);
+    return vec ? launch_one<T, true, kConvAny>(a, B, s, after_producer)
+               : launch_one<T, false, kConvAny>(a, B, s, after_producer);
 }
 
 }  // namespace
 }  // namespace gdn
 
-using namespace gdn;
-
-extern "C" gdn_status gdn_decode_gated(const void* qkv, const void* z, const void* a, const void* b,
-                                       const float* A_log, const float* dt_bias, const float* norm_weight,
-                                       float scale, float* state_inout, void* out, const gdn_dims* d,
-                                       gdn_stream_t stream) {
+gdn_status gdn::decode_gated_checked(const void* qkv, const void* z, const void* a, const void* b,
+                                     const float* A_log, const float* dt_bias, const float* norm_weight, float scale,
+                                     float* state_inout, void* out, const gdn_dims* d, cudaStream_t s,
+                                     bool after_producer, const GatedConvInput* conv) {
     if (!d) return GDN_ERR_NULL;
     if (d->dtype != GDN_F32 && d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
     if (d->flags & ~(uint32_t)GDN_ZERO_INITIAL_STATE) return GDN_ERR_UNSUPPORTED;
@@ -257,7 +314,8 @@ extern "C" gdn_status gdn_decode_gated(const void* qkv, const void* z, const voi
     if (d->Dk > 128 || d->Dv > 128 || d->Hv % d->Hk != 0) return GDN_ERR_DIMS;
     if (d->B * d->Hv > INT32_MAX) return GDN_ERR_DIMS;
     if (d->B == 0) return GDN_OK;
-    if (!qkv || !z || !a || !b || !A_log || !dt_bias || !norm_weight || !state_inout || !out) return GDN_ERR_NULL;
+    if (conv && (d->dtype != GDN_BF16 || !conv->window || !conv->weight || conv->K < 1)) return GDN_ERR_UNSUPPORTED;
+    if ((!qkv && !conv) || !z || !a || !b || !A_log || !dt_bias || !norm_weight || !state_inout || !out) return GDN_ERR_NULL;
     const uintptr_t esz = d->dtype == GDN_BF16 ? 2 : 4;
     if ((reinterpret_cast<uintptr_t>(qkv) | reinterpret_cast<uintptr_t>(z) | reinterpret_cast<uintptr_t>(a) |
          reinterpret_cast<uintptr_t>(b) | reinterpret_cast<uintptr_t>(out)) & (esz - 1))
@@ -266,9 +324,18 @@ extern "C" gdn_status gdn_decode_gated(const void* qkv, const void* z, const voi
          reinterpret_cast<uintptr_t>(norm_weight) | reinterpret_cast<uintptr_t>(state_inout)) & 3u)
         return GDN_ERR_ALIGN;
     GatedArgs g{qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state_inout, out,
-                (int)d->Hk, (int)d->Hv, (int)d->Dk, (int)d->Dv, (d->flags & GDN_ZERO_INITIAL_STATE) ? 1 : 0};
-    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    const cudaError_t e = d->dtype == GDN_BF16 ? launch_gated<__nv_bfloat16>(g, (int)d->B, s)
-                                               : launch_gated<float>(g, (int)d->B, s);
+                (int)d->Hk, (int)d->Hv, (int)d->Dk, (int)d->Dv, (d->flags & GDN_ZERO_INITIAL_STATE) ? 1 : 0,
+                conv ? conv->window : nullptr, conv ? conv->weight : nullptr, conv ? conv->K : 0};
+    const cudaError_t e = conv ? launch_gated_conv(g, (int)d->B, s, after_producer)
+                          : d->dtype == GDN_BF16 ? launch_gated<__nv_bfloat16>(g, (int)d->B, s, after_producer)
+                                                 : launch_gated<float>(g, (int)d->B, s, after_producer);
     return e == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+extern "C" gdn_status gdn_decode_gated(const void* qkv, const void* z, const void* a, const void* b,
+                                       const float* A_log, const float* dt_bias, const float* norm_weight,
+                                       float scale, float* state_inout, void* out, const gdn_dims* d,
+                                       gdn_stream_t stream) {
+    return gdn::decode_gated_checked(qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state_inout, out, d,
+                                     reinterpret_cast<cudaStream_t>(stream), false, nullptr);
 }

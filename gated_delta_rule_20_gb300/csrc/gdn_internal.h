@@ -37,4 +37,23 @@ cudaError_t launch_prefill_ffma(const Problem& p, cudaStream_t stream);
 bool prefill_tc_supported(const Problem& p);
 gdn_status launch_prefill_tc(const Problem& p, int* status_word, cudaStream_t stream);
 
+// The conv1d decode step folded into the gated step: q|k|v are computed from the
+// already shifted windows [B, conv_dim, K] bf16 (the newest token last) and the
+// taps [conv_dim, K] fp32 instead of being read.
+struct GatedConvInput {
+    const void* window;
+    const float* weight;
+    int K;
+};
+
+// gdn_decode_gated after its argument checks (qkv unused when conv is given;
+// conv requires bf16).  With after_producer the kernel is launched with
+// programmatic stream serialization: it may start while the preceding kernel of
+// the stream runs (that kernel must execute griddepcontrol.launch_dependents),
+// and reads nothing but the state before that kernel has completed.
+gdn_status decode_gated_checked(const void* qkv, const void* z, const void* a, const void* b, const float* A_log,
+                                const float* dt_bias, const float* norm_weight, float scale, float* state_inout,
+                                void* out, const gdn_dims* d, cudaStream_t stream, bool after_producer,
+                                const GatedConvInput* conv);
+
 }  // namespace gdn

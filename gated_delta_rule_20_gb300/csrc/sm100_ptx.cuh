@@ -161,8 +161,21 @@ __device__ __forceinline__ void stmatrix_x4_trans(uint32_t addr, uint32_t m0, ui
 __device__ __forceinline__ void cp_async_4(void* dst_smem, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async_8(void* dst_smem, const void* src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst_smem)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+// Programmatic dependent launch.  launch_dependents lets the next kernel of the
+// stream, when it was launched with programmatic stream serialization, start
+// once every CTA of this grid has executed it or exited; griddep_wait blocks
+// until the preceding grid has completed and its writes are visible (it returns
+// at once in a kernel launched without that attribute).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 // 3-D tiled store shared -> global (rows outside the tensor are clipped).
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int c0, int c1, int c2) {
     asm volatile(

@@ -220,8 +220,8 @@ typedef struct {
     uint32_t flags;  /* 0 */
 } gdn_block_dims;
 
-/* Device workspace bytes gdn_decode_block needs (the inter-stage activations:
- * the q|k|v projection and its conv output, z, a, b in bf16); 0 for invalid dims. */
+/* Device workspace bytes gdn_decode_block needs (the inter-stage activations z,
+ * a, b in bf16); 0 for invalid dims. */
 size_t gdn_decode_block_workspace_bytes(const gdn_block_dims* dims);
 
 /*
@@ -235,8 +235,12 @@ size_t gdn_decode_block_workspace_bytes(const gdn_block_dims* dims);
  *   out               [B, 1, value_dim] bf16, the RMSNormGated output
  *   workspace         device memory of at least gdn_decode_block_workspace_bytes,
  *                     16-byte aligned, owned by the caller (else GDN_ERR_DIMS)
- * hidden, the weights and the workspace must be 16-byte aligned (GDN_ERR_ALIGN).
- * Launches three kernels on `stream`.
+ * hidden, the weights and the workspace must be 16-byte aligned, every other
+ * pointer aligned to its element (GDN_ERR_ALIGN); all checks run before the
+ * first launch.  Launches two kernels on `stream`: the projections (whose
+ * q|k|v epilogue shifts the conv windows in place), then the gated step, which
+ * takes the conv1d output from the shifted windows and starts loading the state
+ * while the projections run (programmatic dependent launch).
  */
 gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, const void* W_z, const void* W_a,
                             const void* W_b, const float* conv_weight, void* conv_state_inout,

@@ -62,3 +62,30 @@ def test_block_workspace_too_small_is_refused(gdn):
         gdn.decode_block(x["hidden"], x["W_qkv"], x["W_z"], x["W_a"], x["W_b"], x["conv_weight"], x["conv_state"],
                          x["A_log"], x["dt_bias"], x["norm_weight"], x["state"], 2, 8, 64, 64, workspace=ws)
     assert e.value.code == gdn.GDN_ERR_DIMS
+
+
+def test_block_three_tokens_in_a_row(gdn):
+    """Three calls back to back on one stream, each feeding the next through the conv
+    window and the state: the gated step of a call starts while that call's projections
+    still run, so this checks that it reads their outputs, and the previous call's state,
+    only once they are complete."""
+    w = workloads.BlockWorkload("t", 64, 2048, 16, 32, 128, 128, 4, seed=21)
+    x = workloads.make_block_inputs(w, device="cuda")
+    gen = torch.Generator(device="cpu").manual_seed(22)
+    hiddens = [x["hidden"]] + [torch.randn(x["hidden"].shape, generator=gen).to(torch.bfloat16).cuda()
+                               for _ in range(2)]
+    cst, st = x["conv_state"].clone(), x["state"].clone()
+    outs = []
+    for h in hiddens:
+        out, cst, st = gdn.decode_block(h, x["W_qkv"], x["W_z"], x["W_a"], x["W_b"], x["conv_weight"], cst,
+                                        x["A_log"], x["dt_bias"], x["norm_weight"], st, 16, 32, 128, 128)
+        outs.append(out.clone())
+    torch.cuda.synchronize()
+    rc, rs = x["conv_state"], x["state"]
+    for i, h in enumerate(hiddens):
+        ro, rc, rs = ob.decode_block(h, x["W_qkv"], x["W_z"], x["W_a"], x["W_b"], x["conv_weight"], rc,
+                                     x["A_log"], x["dt_bias"], x["norm_weight"], rs, 16, 32, 128, 128)
+        e = _rel(outs[i], ro)
+        assert e <= 1e-2, "token %d: out rel L2 %.3e" % (i, e)
+    assert _rel(cst, rc) <= 1e-2 and _rel(st, rs) <= 1e-2
+    assert gdn.device_status(0) == 0
