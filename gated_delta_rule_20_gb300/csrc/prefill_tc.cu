@@ -233,18 +233,25 @@ __device__ __forceinline__ void store_t12_frag(uint8_t* t12, const float* bet, c
 }
 
 // Level 0: diagonal 16 x 16 block `blk` of T = (I + A)^-1 by forward
-// substitution, one column per lane (lanes 16..31 repeat lanes 0..15).  Column
-// oriented: once x[m] is final it is eliminated from every later row, so the
-// dependent chain is one FMA per row.
+// substitution, one column per lane (lanes 16..31 repeat lanes 0..15):
+// x_i = delta_ij - sum_{m < i} A_im x_m, the sum taken in the order m = 0, 1, ...,
+// so that x_i is one FMA behind x_{i-1}.  Row i of A is read as 16-byte vectors
+// (the same address in every lane).
 __device__ __forceinline__ void solve_diag_block(float* M, int blk, int lane) {
     const int base = blk * 16, j = lane & 15;
     float x[16];
 #pragma unroll
-    for (int i = 0; i < 16; ++i) x[i] = (i == j) ? 1.f : 0.f;
+    for (int i = 0; i < 16; ++i) {
+        float acc = (i == j) ? 1.f : 0.f;
 #pragma unroll
-    for (int m = 0; m < 15; ++m) {
-#pragma unroll
-        for (int i = m + 1; i < 16; ++i) x[i] = fmaf(-M[(base + i) * AT_STRIDE + base + m], x[m], x[i]);
+        for (int m4 = 0; m4 < i; m4 += 4) {
+            const float4 a = *reinterpret_cast<const float4*>(M + (base + i) * AT_STRIDE + base + m4);
+            acc = fmaf(-a.x, x[m4], acc);
+            if (m4 + 1 < i) acc = fmaf(-a.y, x[m4 + 1], acc);
+            if (m4 + 2 < i) acc = fmaf(-a.z, x[m4 + 2], acc);
+            if (m4 + 3 < i) acc = fmaf(-a.w, x[m4 + 3], acc);
+        }
+        x[i] = acc;
     }
     __syncwarp();
     if (lane < 16) {
