@@ -439,39 +439,62 @@ def run_ours(args, rank, world, local_rank):
     del xb, bws, bout, flush
 
     # ---------------- end to end through the public API from pinned host buffers
+    # Every step copies its inputs and initial state from pinned host memory, runs gdn_prefill
+    # and copies out and the final state back.  The copies of one step overlap the kernel and the
+    # copies of its neighbours (three streams, device buffers double-buffered), as a serving loop
+    # would run them; every byte of every step still crosses the link inside the timed region.
     xh = {k: (v.to("cpu").pin_memory() if hasattr(v, "to") and v is not None else v) for k, v in x.items()}
     st_h = xh["state"].clone().pin_memory()
     out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
     st_back = torch.empty(st_h.shape, dtype=torch.float32).pin_memory()
-    dq, dk, dv = torch.empty_like(x["q"]), torch.empty_like(x["k"]), torch.empty_like(x["v"])
-    dg, db, dst = torch.empty_like(x["g_log"]), torch.empty_like(x["beta"]), torch.empty_like(state)
+    bufs = [dict(q=torch.empty_like(x["q"]), k=torch.empty_like(x["k"]), v=torch.empty_like(x["v"]),
+                 g=torch.empty_like(x["g_log"]), b=torch.empty_like(x["beta"]), st=torch.empty_like(state),
+                 out=torch.empty_like(out)) for _ in range(2)]
     h2d = sum(t.numel() * t.element_size() for t in (xh["q"], xh["k"], xh["v"], xh["g_log"], xh["beta"], st_h))
     d2h = out_h.numel() * out_h.element_size() + st_back.numel() * 4
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    d2h_done = [None, None]
 
-    def e2e_step():
-        for d_, h_ in ((dq, xh["q"]), (dk, xh["k"]), (dv, xh["v"]), (dg, xh["g_log"]), (db, xh["beta"]),
-                       (dst, st_h)):
-            d_.copy_(h_, non_blocking=True)
-        gdn.prefill(dq, dk, dv, dg, db, x["scale"], dst, out, stream=stream)
-        out_h.copy_(out, non_blocking=True)
-        st_back.copy_(dst, non_blocking=True)
+    def e2e_step(i):
+        bf = bufs[i & 1]
+        with torch.cuda.stream(s_in):
+            if d2h_done[i & 1] is not None:  # step i - 2 has read this buffer's out and state back
+                s_in.wait_event(d2h_done[i & 1])
+            for key, h_ in (("q", xh["q"]), ("k", xh["k"]), ("v", xh["v"]), ("g", xh["g_log"]), ("b", xh["beta"]),
+                            ("st", st_h)):
+                bf[key].copy_(h_, non_blocking=True)
+            in_done = torch.cuda.Event()
+            in_done.record(s_in)
+        stream.wait_event(in_done)
+        gdn.prefill(bf["q"], bf["k"], bf["v"], bf["g"], bf["b"], x["scale"], bf["st"], bf["out"], stream=stream)
+        k_done = torch.cuda.Event()
+        k_done.record(stream)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(k_done)
+            out_h.copy_(bf["out"], non_blocking=True)
+            st_back.copy_(bf["st"], non_blocking=True)
+            d2h_done[i & 1] = torch.cuda.Event()
+            d2h_done[i & 1].record(s_out)
 
-    for _ in range(max(args.warmup, 3)):
-        e2e_step()
+    for i in range(max(args.warmup, 3)):
+        e2e_step(i)
     torch.cuda.synchronize()
+    d2h_done[0] = d2h_done[1] = None
     barrier()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e2e_steps = max(1, min(args.steps, 10))
+    e2e_steps = max(1, min(args.steps, 30))
     torch.cuda.synchronize()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    stream.wait_event(d2h_done[(e2e_steps - 1) & 1])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     e2e = {"value": weak_scaling_value(w.B * w.S, world, e2e_ms), "unit": "tokens/s", "ms_per_step": e2e_ms,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+           "overlap": "copies of neighbouring steps overlap the kernel (3 streams, double-buffered device inputs)"}
     if gdn.device_status(local_rank) != 0:
         raise RuntimeError("a kernel reported a wait timeout")
 
