@@ -39,6 +39,8 @@ KERNEL_SOURCES = {
     "conv1d_decode_k4_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
     "gdn_decode_gated_kernel": "gated_delta_rule_20_gb300/csrc/decode_gated.cu",
     "inproj_gemm_kernel": "gated_delta_rule_20_gb300/csrc/block.cu",
+    # the two kernels of one decode-block call; the sha covers both files, in this order
+    "decode_block": ("gated_delta_rule_20_gb300/csrc/block.cu", "gated_delta_rule_20_gb300/csrc/decode_gated.cu"),
 }
 
 
@@ -111,8 +113,9 @@ def recorded_traffic(kernel: str):
     import hashlib
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
-    src = os.path.join(ROOT, KERNEL_SOURCES[kernel])
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+    srcs = KERNEL_SOURCES[kernel]
+    srcs = (srcs,) if isinstance(srcs, str) else srcs
+    sha = hashlib.sha256(b"".join(open(os.path.join(ROOT, f), "rb").read() for f in srcs)).hexdigest()[:16]
     for line in open(PROFILE_TRAFFIC):
         parts = line.strip().strip("|").split("|")
         parts = [p.strip() for p in parts]
@@ -433,7 +436,7 @@ def run_ours(args, rank, world, local_rank):
     block = {"workload": wb.name, "ms": bms, "tokens_per_s": wb.B / (bms * 1e-3) * world, "kernels": 2,
              "l2": "flushed (256 MiB write) before every call",
              "roofline": {"bound": "hbm", "achieved": bb / (bms * 1e-3) / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
-                          "frac": bb / (bms * 1e-3) / 1e9 / peaks["hbm"], "traffic": None,
+                          "frac": bb / (bms * 1e-3) / 1e9 / peaks["hbm"], "traffic": recorded_traffic("decode_block"),
                           "kernel": "inproj_gemm_kernel + gdn_decode_gated_kernel",
                           "algorithmic_bytes_per_call": bb}}
     del xb, bws, bout, flush
