@@ -19,6 +19,7 @@
 #include <cuda_runtime.h>
 
 #include <cstdint>
+#include <mutex>
 
 #include "gdn_internal.h"
 #include "sm100_ptx.cuh"
@@ -78,6 +79,7 @@ struct GatedArgs {
     const void* conv_win;
     const float* conv_w;
     int K;
+    int32_t* status;  // device status word: a wait that gave up records GDN_ERR_TIMEOUT
 };
 
 // How the kernel gets q, k and v: kDirect reads them; kConv4 / kConvAny compute the
@@ -86,18 +88,23 @@ enum InputMode { kDirect = 0, kConv4 = 1, kConvAny = 2 };
 
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
+// conv1d decode output of one channel from its shifted window (4 bf16, oldest first, in one
+// 8-byte word) and its taps, rounded to bf16 as the stand-alone conv step stores it
+__device__ __forceinline__ float conv4_value(uint2 s, float4 w) {
+    float z = fmaf(w.x, __uint_as_float(s.x << 16), 0.f);
+    z = fmaf(w.y, __uint_as_float(s.x & 0xffff0000u), z);
+    z = fmaf(w.z, __uint_as_float(s.y << 16), z);
+    z = fmaf(w.w, __uint_as_float(s.y & 0xffff0000u), z);
+    return __bfloat162float(__float2bfloat16_rn(silu_fast(z)));
+}
+
 template <typename T, int kMode>
 __device__ __forceinline__ float input_value(const GatedArgs& p, const T* row_in, long long row, long long ch) {
     if constexpr (kMode == kDirect) {
         return to_f32(row_in[ch]);
     } else if constexpr (kMode == kConv4) {
-        const uint2 s = reinterpret_cast<const uint2*>(p.conv_win)[row + ch];
-        const float4 w = reinterpret_cast<const float4*>(p.conv_w)[ch];
-        float z = fmaf(w.x, __uint_as_float(s.x << 16), 0.f);
-        z = fmaf(w.y, __uint_as_float(s.x & 0xffff0000u), z);
-        z = fmaf(w.z, __uint_as_float(s.y << 16), z);
-        z = fmaf(w.w, __uint_as_float(s.y & 0xffff0000u), z);
-        return __bfloat162float(__float2bfloat16_rn(silu_fast(z)));
+        return conv4_value(reinterpret_cast<const uint2*>(p.conv_win)[row + ch],
+                           reinterpret_cast<const float4*>(p.conv_w)[ch]);
     } else {
         const __nv_bfloat16* s = static_cast<const __nv_bfloat16*>(p.conv_win) + (row + ch) * p.K;
         const float* w = p.conv_w + ch * p.K;
@@ -107,64 +114,34 @@ __device__ __forceinline__ float input_value(const GatedArgs& p, const T* row_in
     }
 }
 
-template <typename T, bool kVec, int kMode>
-__global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs p) {
-    __shared__ float s_k[128], s_q[128];  // raw q and k; their norms are applied to the reductions
-    __shared__ float s_red[2][kRowGroups][128];
-    __shared__ float s_d[128];
-    __shared__ float s_v[128], s_gate[128];  // v, and norm_weight * silu(z)
-    __shared__ float s_part[4][kThreads / 32];  // per-warp partial sums: |q|^2, |k|^2, k.q, sum o^2
+// Per-head scratch of the step (shared memory).
+struct GatedShared {
+    float s_k[128], s_q[128];  // raw q and k; their norms are applied to the reductions
+    float s_red[2][kRowGroups][128];
+    float s_d[128];
+    float s_v[128], s_gate[128];  // v, and norm_weight * silu(z)
+    float s_part[4][kThreads / 32];  // per-warp partial sums: |q|^2, |k|^2, k.q, sum o^2
+};
 
-    const int bh = blockIdx.x;
-    const int Hv = p.Hv, Dk = p.Dk, Dv = p.Dv;
-    const int b = bh / Hv, h = bh - b * Hv;
-    const int hk = h / (Hv / p.Hk);
+// One head once its inputs are at hand: the state in registers (thread (rg, cg) holds rows
+// rg + 8 i, columns 4 cg .. 4 cg + 3), raw q and k in registers (thread < Dk), v and
+// norm_weight * silu(z) in sh.s_v / sh.s_gate (thread < Dv, written before the call), the raw
+// gate inputs.  Computes the step, stores the new state in place and the gated output.
+template <typename T, bool kVec>
+__device__ __forceinline__ void gated_head(const GatedArgs& p, GatedShared& sh, int bh, float4 (&S)[kMaxRows],
+                                           float qv, float kv, float a_in, float b_in, float A_log, float dt_bias) {
+    float* s_k = sh.s_k;
+    float* s_q = sh.s_q;
+    auto& s_red = sh.s_red;
+    float* s_d = sh.s_d;
+    float* s_v = sh.s_v;
+    float* s_gate = sh.s_gate;
+    auto& s_part = sh.s_part;
+    const int Dk = p.Dk, Dv = p.Dv;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int cg = tid & (kColGroups - 1), rg = tid >> 5;
     const int c0 = cg * 4;
-    const long long conv_dim = 2LL * p.Hk * Dk + (long long)Hv * Dv;
-    const T* row_in = static_cast<const T*>(p.qkv) + b * conv_dim;  // kDirect
-    const long long row = (long long)b * conv_dim;                     // conv modes
-    const long long ch_q = (long long)hk * Dk, ch_k = (long long)p.Hk * Dk + ch_q;
-    const long long ch_v = 2LL * p.Hk * Dk + (long long)h * Dv;
     float* Sp = p.state + (long long)bh * Dk * Dv;
-
-    // the state loads go out first: they are the bulk of the traffic
-    float4 S[kMaxRows];
-#pragma unroll
-    for (int i = 0; i < kMaxRows; ++i) {
-        const int r = rg + i * kRowGroups;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (!p.zero_init && r < Dk) {
-            if (kVec) {
-                if (c0 < Dv) x = __ldcs(reinterpret_cast<const float4*>(Sp + (long long)r * Dv + c0));
-            } else {
-                const float* row = Sp + (long long)r * Dv;
-                if (c0 + 0 < Dv) x.x = row[c0 + 0];
-                if (c0 + 1 < Dv) x.y = row[c0 + 1];
-                if (c0 + 2 < Dv) x.z = row[c0 + 2];
-                if (c0 + 3 < Dv) x.w = row[c0 + 3];
-            }
-        }
-        S[i] = x;
-    }
-    // Behind a programmatic launch the loads above overlap the producer of the
-    // inputs below (the decode block's projection kernel); the state is not its output.
-    ptx::griddep_wait();
-
-    // every other input of the head is fetched now too, so that no load waits behind a barrier
-    float qv = 0.f, kv = 0.f;
-    if (tid < Dk) {
-        qv = input_value<T, kMode>(p, row_in, row, ch_q + tid);
-        kv = input_value<T, kMode>(p, row_in, row, ch_k + tid);
-    }
-    if (tid < Dv) {
-        const float zv = to_f32(static_cast<const T*>(p.z)[(long long)bh * Dv + tid]);
-        s_v[tid] = input_value<T, kMode>(p, row_in, row, ch_v + tid);
-        s_gate[tid] = p.norm_weight[tid] * (zv / (1.f + expf(-zv)));
-    }
-    const float a_in = to_f32(static_cast<const T*>(p.a)[bh]), b_in = to_f32(static_cast<const T*>(p.b)[bh]);
-    const float A_log = p.A_log[h], dt_bias = p.dt_bias[h];
 
     if (tid < Dk) {
         s_q[tid] = qv;
@@ -267,6 +244,235 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs
     }
 }
 
+
+template <typename T, bool kVec, int kMode>
+__global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_kernel(GatedArgs p) {
+    __shared__ GatedShared sh;
+    const int bh = blockIdx.x;
+    const int Hv = p.Hv, Dk = p.Dk, Dv = p.Dv;
+    const int b = bh / Hv, h = bh - b * Hv;
+    const int hk = h / (Hv / p.Hk);
+    const int tid = threadIdx.x;
+    const int cg = tid & (kColGroups - 1), rg = tid >> 5;
+    const int c0 = cg * 4;
+    const long long conv_dim = 2LL * p.Hk * Dk + (long long)Hv * Dv;
+    const T* row_in = static_cast<const T*>(p.qkv) + b * conv_dim;  // kDirect
+    const long long row = (long long)b * conv_dim;                     // conv modes
+    const long long ch_q = (long long)hk * Dk, ch_k = (long long)p.Hk * Dk + ch_q;
+    const long long ch_v = 2LL * p.Hk * Dk + (long long)h * Dv;
+    const float* Sp = p.state + (long long)bh * Dk * Dv;
+
+    // the state loads go out first: they are the bulk of the traffic
+    float4 S[kMaxRows];
+#pragma unroll
+    for (int i = 0; i < kMaxRows; ++i) {
+        const int r = rg + i * kRowGroups;
+        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (!p.zero_init && r < Dk) {
+            if (kVec) {
+                if (c0 < Dv) x = __ldcs(reinterpret_cast<const float4*>(Sp + (long long)r * Dv + c0));
+            } else {
+                const float* rowp = Sp + (long long)r * Dv;
+                if (c0 + 0 < Dv) x.x = rowp[c0 + 0];
+                if (c0 + 1 < Dv) x.y = rowp[c0 + 1];
+                if (c0 + 2 < Dv) x.z = rowp[c0 + 2];
+                if (c0 + 3 < Dv) x.w = rowp[c0 + 3];
+            }
+        }
+        S[i] = x;
+    }
+    // Behind a programmatic launch the loads above overlap the producer of the
+    // inputs below (the decode block's projection kernel); the state is not its output.
+    ptx::griddep_wait();
+
+    // every other input of the head is fetched now too, so that no load waits behind a barrier
+    float qv = 0.f, kv = 0.f;
+    if (tid < Dk) {
+        qv = input_value<T, kMode>(p, row_in, row, ch_q + tid);
+        kv = input_value<T, kMode>(p, row_in, row, ch_k + tid);
+    }
+    if (tid < Dv) {
+        const float zv = to_f32(static_cast<const T*>(p.z)[(long long)bh * Dv + tid]);
+        sh.s_v[tid] = input_value<T, kMode>(p, row_in, row, ch_v + tid);
+        sh.s_gate[tid] = p.norm_weight[tid] * (zv / (1.f + expf(-zv)));
+    }
+    const float a_in = to_f32(static_cast<const T*>(p.a)[bh]), b_in = to_f32(static_cast<const T*>(p.b)[bh]);
+    gated_head<T, kVec>(p, sh, bh, S, qv, kv, a_in, b_in, p.A_log[h], p.dt_bias[h]);
+}
+
+// Dk = Dv = 128 with 16-byte aligned state and input rows: persistent CTAs, two per SM,
+// walk the heads blockIdx.x, blockIdx.x + gridDim.x, ...  A head's state (64 KB) reaches
+// shared memory in one bulk copy and its other inputs in 16-byte asynchronous copies, both
+// issued as soon as the previous head has been read out of shared memory, so that the
+// memory system holds the next head's bytes while the CTA computes.  The step itself is
+// gated_head, as in gdn_decode_gated_kernel.
+constexpr int kSD = 128;
+constexpr uint32_t kStreamStateBytes = kSD * kSD * 4;
+constexpr uint32_t kStreamInBytes = 9984;  // the largest input set (conv mode, below)
+
+struct StreamSmem {
+    float state[kSD * kSD];
+    alignas(16) uint8_t in[kStreamInBytes];
+    uint64_t full;
+    int abort;
+};
+
+// Input buffer of one head.  Direct: q, k, v, z [128] in the compute type at 0, 128, 256,
+// 384 elements, then norm_weight [128] fp32.  Conv mode: the windows of the q, k, v channels
+// [128] uint2 at bytes 0, 1024, 2048, their taps [128] float4 at 3072, 5120, 7168, z [128]
+// bf16 at 9216, norm_weight [128] fp32 at 9472.
+template <typename T, int kMode>
+__device__ __forceinline__ void stream_issue_inputs(const GatedArgs& p, uint8_t* in, int bh) {
+    const int Hv = p.Hv, b = bh / Hv, h = bh - b * Hv, hk = h / (Hv / p.Hk);
+    const long long C = 2LL * p.Hk * kSD + (long long)Hv * kSD;
+    const long long cq = (long long)hk * kSD, ck = (long long)p.Hk * kSD + cq, cv = 2LL * p.Hk * kSD + (long long)h * kSD;
+    const uint8_t* src[8];
+    uint32_t off[8], bytes[8];
+    int n = 0;
+    auto add = [&](const void* sp, uint32_t o, uint32_t nb) {
+        src[n] = static_cast<const uint8_t*>(sp);
+        off[n] = o;
+        bytes[n] = nb;
+        ++n;
+    };
+    if constexpr (kMode == kDirect) {
+        constexpr uint32_t e = sizeof(T);
+        const T* rowp = static_cast<const T*>(p.qkv) + (long long)b * C;
+        add(rowp + cq, 0, kSD * e);
+        add(rowp + ck, kSD * e, kSD * e);
+        add(rowp + cv, 2 * kSD * e, kSD * e);
+        add(static_cast<const T*>(p.z) + (long long)bh * kSD, 3 * kSD * e, kSD * e);
+        add(p.norm_weight, 4 * kSD * e, kSD * 4);
+    } else {
+        const uint2* win = static_cast<const uint2*>(p.conv_win) + (long long)b * C;
+        const float4* taps = reinterpret_cast<const float4*>(p.conv_w);
+        add(win + cq, 0, 1024);
+        add(win + ck, 1024, 1024);
+        add(win + cv, 2048, 1024);
+        add(taps + cq, 3072, 2048);
+        add(taps + ck, 5120, 2048);
+        add(taps + cv, 7168, 2048);
+        add(static_cast<const __nv_bfloat16*>(p.z) + (long long)bh * kSD, 9216, 256);
+        add(p.norm_weight, 9472, 512);
+    }
+    for (int r = 0; r < n; ++r)
+        for (uint32_t i = threadIdx.x; i < bytes[r] / 16; i += kThreads) ptx::cp_async_16(in + off[r] + 16 * i, src[r] + 16 * i);
+    ptx::cp_async_commit();
+}
+
+template <typename T, int kMode>
+__global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_stream_kernel(GatedArgs p, int num_heads) {
+    extern __shared__ __align__(128) uint8_t stream_raw[];
+    StreamSmem& sm = *reinterpret_cast<StreamSmem*>(stream_raw);
+    __shared__ GatedShared sh;
+    const int tid = threadIdx.x;
+    const int cg = tid & (kColGroups - 1), rg = tid >> 5, c0 = cg * 4;
+    const int n_local = (num_heads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
+    auto head_of = [&](int l) { return (int)blockIdx.x + l * (int)gridDim.x; };
+    auto load_state = [&](int bh) {
+        ptx::mbar_arrive_expect_tx(&sm.full, kStreamStateBytes);
+        ptx::bulk_load(sm.state, p.state + (long long)bh * kSD * kSD, kStreamStateBytes, &sm.full);
+    };
+    if (tid == 0) {
+        ptx::mbar_init(&sm.full, 1);
+        sm.abort = 0;
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+    if (tid == 0 && !p.zero_init) load_state(head_of(0));
+    // Behind a programmatic launch the state copy above overlaps the producer of the other
+    // inputs (the decode block's projection kernel); the state is not its output.
+    ptx::griddep_wait();
+    stream_issue_inputs<T, kMode>(p, sm.in, head_of(0));
+    float a_n = to_f32(static_cast<const T*>(p.a)[head_of(0)]), b_n = to_f32(static_cast<const T*>(p.b)[head_of(0)]);
+    float al_n = p.A_log[head_of(0) % p.Hv], dt_n = p.dt_bias[head_of(0) % p.Hv];
+
+    for (int l = 0; l < n_local; ++l) {
+        const int bh = head_of(l);
+        const float a_in = a_n, b_in = b_n, A_log = al_n, dt_bias = dt_n;
+        if (!p.zero_init) (void)ptx::mbar_wait_or_abort(&sm.full, l & 1, &sm.abort);
+        ptx::cp_async_wait_all();
+        __syncthreads();  // every thread's copies have landed; the previous head is done with sh
+        float4 S[kMaxRows];
+#pragma unroll
+        for (int i = 0; i < kMaxRows; ++i)
+            S[i] = p.zero_init ? make_float4(0.f, 0.f, 0.f, 0.f)
+                               : *reinterpret_cast<const float4*>(&sm.state[(rg + i * kRowGroups) * kSD + c0]);
+        float qv = 0.f, kv = 0.f, vv = 0.f, zv = 0.f, nw = 0.f;
+        if (tid < kSD) {
+            if constexpr (kMode == kDirect) {
+                const T* in = reinterpret_cast<const T*>(sm.in);
+                qv = to_f32(in[tid]);
+                kv = to_f32(in[kSD + tid]);
+                vv = to_f32(in[2 * kSD + tid]);
+                zv = to_f32(in[3 * kSD + tid]);
+                nw = reinterpret_cast<const float*>(sm.in + 4 * kSD * sizeof(T))[tid];
+            } else {
+                const uint2* win = reinterpret_cast<const uint2*>(sm.in);
+                const float4* taps = reinterpret_cast<const float4*>(sm.in + 3072);
+                qv = conv4_value(win[tid], taps[tid]);
+                kv = conv4_value(win[kSD + tid], taps[kSD + tid]);
+                vv = conv4_value(win[2 * kSD + tid], taps[2 * kSD + tid]);
+                zv = __bfloat162float(reinterpret_cast<const __nv_bfloat16*>(sm.in + 9216)[tid]);
+                nw = reinterpret_cast<const float*>(sm.in + 9472)[tid];
+            }
+        }
+        __syncthreads();  // the state and the inputs of head l have been read out of shared memory
+        if (l + 1 < n_local) {
+            const int nb = head_of(l + 1);
+            if (tid == 0 && !p.zero_init) load_state(nb);
+            stream_issue_inputs<T, kMode>(p, sm.in, nb);
+            a_n = to_f32(static_cast<const T*>(p.a)[nb]);
+            b_n = to_f32(static_cast<const T*>(p.b)[nb]);
+            al_n = p.A_log[nb % p.Hv];
+            dt_n = p.dt_bias[nb % p.Hv];
+        }
+        if (tid < kSD) {
+            sh.s_v[tid] = vv;
+            sh.s_gate[tid] = nw * (zv / (1.f + expf(-zv)));
+        }
+        gated_head<T, true>(p, sh, bh, S, qv, kv, a_in, b_in, A_log, dt_bias);
+    }
+    __syncthreads();
+    if (tid == 0 && sm.abort) atomicExch(p.status, (int32_t)GDN_ERR_TIMEOUT);
+}
+
+template <typename T, int kMode>
+cudaError_t launch_stream(const GatedArgs& a, int B, cudaStream_t s, bool after_producer) {
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [] {
+        attr_err = cudaFuncSetAttribute(gdn_decode_gated_stream_kernel<T, kMode>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sizeof(StreamSmem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int heads = B * a.Hv;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(heads < 2 * sms ? heads : 2 * sms));
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = sizeof(StreamSmem);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = after_producer ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, gdn_decode_gated_stream_kernel<T, kMode>, a, heads);
+}
+
+// The streaming kernel needs Dk = Dv = 128 and 16-byte aligned state, input rows and taps.
+bool stream_ok(const GatedArgs& a, size_t esz) {
+    const auto al = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
+    const long long C = 2LL * a.Hk * a.Dk + (long long)a.Hv * a.Dv;
+    if (a.Dk != kSD || a.Dv != kSD || !al(a.state) || !al(a.z) || !al(a.norm_weight)) return false;
+    if (a.conv_win) return a.K == 4 && al(a.conv_win) && al(a.conv_w);
+    return al(a.qkv) && (C * (long long)esz) % 16 == 0;
+}
+
 template <typename T, bool kVec, int kMode>
 cudaError_t launch_one(const GatedArgs& a, int B, cudaStream_t s, bool after_producer) {
     cudaLaunchConfig_t cfg = {};
@@ -283,6 +489,7 @@ cudaError_t launch_one(const GatedArgs& a, int B, cudaStream_t s, bool after_pro
 
 template <typename T>
 cudaError_t launch_gated(const GatedArgs& a, int B, cudaStream_t s, bool after_producer) {
+    if (stream_ok(a, sizeof(T))) return launch_stream<T, kDirect>(a, B, s, after_producer);
     const bool vec = (a.Dv % 4) == 0 && (reinterpret_cast<uintptr_t>(a.state) & 15u) == 0;
     return vec ? launch_one<T, true, kDirect>(a, B, s, after_producer)
                : launch_one<T, false, kDirect>(a, B, s, after_producer);
@@ -293,6 +500,7 @@ cudaError_t launch_gated_conv(const GatedArgs& a, int B, cudaStream_t s, bool af
     const bool vec = (a.Dv % 4) == 0 && (reinterpret_cast<uintptr_t>(a.state) & 15u) == 0;
     const bool conv4 = a.K == 4 && (reinterpret_cast<uintptr_t>(a.conv_win) & 7u) == 0 &&
                        (reinterpret_cast<uintptr_t>(a.conv_w) & 15u) == 0;
+    if (conv4 && stream_ok(a, sizeof(T))) return launch_stream<T, kConv4>(a, B, s, after_producer);
     if (conv4)
         return vec ? launch_one<T, true, kConv4>(a, B, s, after_producer)
                    : launch_one<T, false, kConv4>(a, B, s, after_producer);
@@ -325,7 +533,9 @@ gdn_status gdn::decode_gated_checked(const void* qkv, const void* z, const void*
         return GDN_ERR_ALIGN;
     GatedArgs g{qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state_inout, out,
                 (int)d->Hk, (int)d->Hv, (int)d->Dk, (int)d->Dv, (d->flags & GDN_ZERO_INITIAL_STATE) ? 1 : 0,
-                conv ? conv->window : nullptr, conv ? conv->weight : nullptr, conv ? conv->K : 0};
+                conv ? conv->window : nullptr, conv ? conv->weight : nullptr, conv ? conv->K : 0, nullptr};
+    gdn_status sw = status_word_for_current_device(&g.status);
+    if (sw != GDN_OK) return sw;
     const cudaError_t e = conv ? launch_gated_conv(g, (int)d->B, s, after_producer)
                           : d->dtype == GDN_BF16 ? launch_gated<__nv_bfloat16>(g, (int)d->B, s, after_producer)
                                                  : launch_gated<float>(g, (int)d->B, s, after_producer);
