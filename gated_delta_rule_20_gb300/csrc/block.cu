@@ -56,6 +56,7 @@ struct GemmArgs {
     int N[kMaxGroups];
     __nv_bfloat16* conv_state;    // [B][N_0][K]: group 0's conv windows, shifted in place
     int K, conv_vec4;             // conv_vec4: K == 4 with 8-byte windows
+    int* head_counter;            // the gated step's head counter, zeroed here
     int tile_start[kMaxGroups + 1];
     int B, H, nb, npad;           // nb = hidden boxes of 64 rows; npad = MMA N
     int stages;                   // pipeline depth, <= kMaxStages
@@ -84,6 +85,7 @@ __global__ void __launch_bounds__(kGThreads, 2)
     volatile int* abort_flag = &bars->abort;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     ptx::griddep_launch_dependents();  // the gated step may start its state loads now
+    if (blockIdx.x == 0 && tid == 0) *args.head_counter = 0;  // read by the gated step after this grid completes
 
     int g = 0;  // weight matrix of this CTA
     while (g + 1 < kMaxGroups && (int)blockIdx.x >= args.tile_start[g + 1]) ++g;
@@ -257,7 +259,7 @@ bool encode_2d(CUtensorMap* map, const void* ptr, long long rows, long long cols
 
 struct BlockLayout {
     long long C, VD;           // conv_dim, value_dim
-    size_t off_z, off_a, off_b, bytes;
+    size_t off_z, off_a, off_b, off_ctr, bytes;
 };
 
 BlockLayout layout(const gdn_block_dims* d) {
@@ -269,6 +271,7 @@ BlockLayout layout(const gdn_block_dims* d) {
     L.off_z = o;    o = up(o + (size_t)d->B * L.VD * 2);
     L.off_a = o;    o = up(o + (size_t)d->B * d->Hv * 2);
     L.off_b = o;    o = up(o + (size_t)d->B * d->Hv * 2);
+    L.off_ctr = o;  o = up(o + sizeof(int));
     L.bytes = o;
     return L;
 }
@@ -338,6 +341,7 @@ extern "C" gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, co
     }
     a.tile_start[kMaxGroups] = tiles;
     a.conv_state = static_cast<__nv_bfloat16*>(conv_state_inout);
+    a.head_counter = reinterpret_cast<int*>(ws + L.off_ctr);
     a.K = (int)d->K;
     a.conv_vec4 = d->K == 4 && (reinterpret_cast<uintptr_t>(conv_state_inout) & 7u) == 0;
     a.B = (int)d->B;
@@ -372,5 +376,6 @@ extern "C" gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, co
     const gdn_dims gd{d->B, d->Hk, d->Hv, 1, d->Dk, d->Dv, GDN_BF16, 0};
     const GatedConvInput conv{conv_state_inout, conv_weight, (int)d->K};
     return decode_gated_checked(nullptr, ws + L.off_z, ws + L.off_a, ws + L.off_b, A_log, dt_bias, norm_weight,
-                                1.0f / std::sqrt((float)d->Dk), state_inout, out, &gd, s, true, &conv);
+                                1.0f / std::sqrt((float)d->Dk), state_inout, out, &gd, s, true, &conv,
+                                reinterpret_cast<int*>(ws + L.off_ctr));
 }

@@ -80,6 +80,10 @@ struct GatedArgs {
     const float* conv_w;
     int K;
     int32_t* status;  // device status word: a wait that gave up records GDN_ERR_TIMEOUT
+    // Streaming kernel: when set, heads after each CTA's first are taken from this counter
+    // (zero when the kernel starts reading it; advanced by one per head taken), so that CTAs
+    // that start early take more heads.  When null, CTA i takes heads i, i + gridDim.x, ...
+    int* next_head;
 };
 
 // How the kernel gets q, k and v: kDirect reads them; kConv4 / kConvAny compute the
@@ -367,28 +371,27 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_stream_kernel(Ga
     __shared__ GatedShared sh;
     const int tid = threadIdx.x;
     const int cg = tid & (kColGroups - 1), rg = tid >> 5, c0 = cg * 4;
-    const int n_local = (num_heads - (int)blockIdx.x + (int)gridDim.x - 1) / (int)gridDim.x;
-    auto head_of = [&](int l) { return (int)blockIdx.x + l * (int)gridDim.x; };
     auto load_state = [&](int bh) {
         ptx::mbar_arrive_expect_tx(&sm.full, kStreamStateBytes);
         ptx::bulk_load(sm.state, p.state + (long long)bh * kSD * kSD, kStreamStateBytes, &sm.full);
     };
+    __shared__ int s_next;
     if (tid == 0) {
         ptx::mbar_init(&sm.full, 1);
         sm.abort = 0;
         ptx::fence_mbar_init();
     }
     __syncthreads();
-    if (tid == 0 && !p.zero_init) load_state(head_of(0));
+    int bh = (int)blockIdx.x;  // the CTA's first head (the grid has at most num_heads CTAs)
+    if (tid == 0 && !p.zero_init) load_state(bh);
     // Behind a programmatic launch the state copy above overlaps the producer of the other
     // inputs (the decode block's projection kernel); the state is not its output.
     ptx::griddep_wait();
-    stream_issue_inputs<T, kMode>(p, sm.in, head_of(0));
-    float a_n = to_f32(static_cast<const T*>(p.a)[head_of(0)]), b_n = to_f32(static_cast<const T*>(p.b)[head_of(0)]);
-    float al_n = p.A_log[head_of(0) % p.Hv], dt_n = p.dt_bias[head_of(0) % p.Hv];
+    stream_issue_inputs<T, kMode>(p, sm.in, bh);
+    float a_n = to_f32(static_cast<const T*>(p.a)[bh]), b_n = to_f32(static_cast<const T*>(p.b)[bh]);
+    float al_n = p.A_log[bh % p.Hv], dt_n = p.dt_bias[bh % p.Hv];
 
-    for (int l = 0; l < n_local; ++l) {
-        const int bh = head_of(l);
+    for (int l = 0;; ++l) {
         const float a_in = a_n, b_in = b_n, A_log = al_n, dt_bias = dt_n;
         if (!p.zero_init) (void)ptx::mbar_wait_or_abort(&sm.full, l & 1, &sm.abort);
         ptx::cp_async_wait_all();
@@ -417,9 +420,10 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_stream_kernel(Ga
                 nw = reinterpret_cast<const float*>(sm.in + 9472)[tid];
             }
         }
-        __syncthreads();  // the state and the inputs of head l have been read out of shared memory
-        if (l + 1 < n_local) {
-            const int nb = head_of(l + 1);
+        if (tid == 0) s_next = p.next_head ? atomicAdd(p.next_head, 1) + (int)gridDim.x : bh + (int)gridDim.x;
+        __syncthreads();  // the state and the inputs of this head have been read out of shared memory
+        const int nb = s_next;
+        if (nb < num_heads) {
             if (tid == 0 && !p.zero_init) load_state(nb);
             stream_issue_inputs<T, kMode>(p, sm.in, nb);
             a_n = to_f32(static_cast<const T*>(p.a)[nb]);
@@ -432,6 +436,8 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_stream_kernel(Ga
             sh.s_gate[tid] = nw * (zv / (1.f + expf(-zv)));
         }
         gated_head<T, true>(p, sh, bh, S, qv, kv, a_in, b_in, A_log, dt_bias);
+        if (nb >= num_heads) break;
+        bh = nb;
     }
     __syncthreads();
     if (tid == 0 && sm.abort) atomicExch(p.status, (int32_t)GDN_ERR_TIMEOUT);
@@ -514,7 +520,7 @@ cudaError_t launch_gated_conv(const GatedArgs& a, int B, cudaStream_t s, bool af
 gdn_status gdn::decode_gated_checked(const void* qkv, const void* z, const void* a, const void* b,
                                      const float* A_log, const float* dt_bias, const float* norm_weight, float scale,
                                      float* state_inout, void* out, const gdn_dims* d, cudaStream_t s,
-                                     bool after_producer, const GatedConvInput* conv) {
+                                     bool after_producer, const GatedConvInput* conv, int* next_head) {
     if (!d) return GDN_ERR_NULL;
     if (d->dtype != GDN_F32 && d->dtype != GDN_BF16) return GDN_ERR_UNSUPPORTED;
     if (d->flags & ~(uint32_t)GDN_ZERO_INITIAL_STATE) return GDN_ERR_UNSUPPORTED;
@@ -533,7 +539,7 @@ gdn_status gdn::decode_gated_checked(const void* qkv, const void* z, const void*
         return GDN_ERR_ALIGN;
     GatedArgs g{qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state_inout, out,
                 (int)d->Hk, (int)d->Hv, (int)d->Dk, (int)d->Dv, (d->flags & GDN_ZERO_INITIAL_STATE) ? 1 : 0,
-                conv ? conv->window : nullptr, conv ? conv->weight : nullptr, conv ? conv->K : 0, nullptr};
+                conv ? conv->window : nullptr, conv ? conv->weight : nullptr, conv ? conv->K : 0, nullptr, next_head};
     gdn_status sw = status_word_for_current_device(&g.status);
     if (sw != GDN_OK) return sw;
     const cudaError_t e = conv ? launch_gated_conv(g, (int)d->B, s, after_producer)
@@ -547,5 +553,5 @@ extern "C" gdn_status gdn_decode_gated(const void* qkv, const void* z, const voi
                                        float scale, float* state_inout, void* out, const gdn_dims* d,
                                        gdn_stream_t stream) {
     return gdn::decode_gated_checked(qkv, z, a, b, A_log, dt_bias, norm_weight, scale, state_inout, out, d,
-                                     reinterpret_cast<cudaStream_t>(stream), false, nullptr);
+                                     reinterpret_cast<cudaStream_t>(stream), false, nullptr, nullptr);
 }

@@ -50,10 +50,12 @@ struct GatedConvInput {
 // conv requires bf16).  With after_producer the kernel is launched with
 // programmatic stream serialization: it may start while the preceding kernel of
 // the stream runs (that kernel must execute griddepcontrol.launch_dependents),
-// and reads nothing but the state before that kernel has completed.
+// and reads nothing but the state before that kernel has completed.  next_head,
+// when not null, is a device counter that is zero once the preceding kernel has
+// completed: the streaming kernel then hands out heads dynamically.
 gdn_status decode_gated_checked(const void* qkv, const void* z, const void* a, const void* b, const float* A_log,
                                 const float* dt_bias, const float* norm_weight, float scale, float* state_inout,
                                 void* out, const gdn_dims* d, cudaStream_t stream, bool after_producer,
-                                const GatedConvInput* conv);
+                                const GatedConvInput* conv, int* next_head);
 
 }  // namespace gdn

@@ -221,7 +221,7 @@ typedef struct {
 } gdn_block_dims;
 
 /* Device workspace bytes gdn_decode_block needs (the inter-stage activations z,
- * a, b in bf16); 0 for invalid dims. */
+ * a, b in bf16, and a work counter of the gated step); 0 for invalid dims. */
 size_t gdn_decode_block_workspace_bytes(const gdn_block_dims* dims);
 
 /*
