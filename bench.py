@@ -34,10 +34,10 @@ DECODE = workloads.DECODE_STEP
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "dram_traffic.md")
 KERNEL_SOURCES = {
     "gdn_prefill_tc_kernel": "gated_delta_rule_20_gb300/csrc/prefill_tc.cu",
-    "gdn_decode_kernel": "gated_delta_rule_20_gb300/csrc/decode.cu",
+    "gdn_decode_stream_kernel": "gated_delta_rule_20_gb300/csrc/decode.cu",
     "conv1d_prefill_vec8_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
     "conv1d_decode_k4_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
-    "gdn_decode_gated_kernel": "gated_delta_rule_20_gb300/csrc/decode_gated.cu",
+    "gdn_decode_gated_stream_kernel": "gated_delta_rule_20_gb300/csrc/decode_gated.cu",
     "inproj_gemm_kernel": "gated_delta_rule_20_gb300/csrc/block.cu",
     # the two kernels of one decode-block call; the sha covers both files, in this order
     "decode_block": ("gated_delta_rule_20_gb300/csrc/block.cu", "gated_delta_rule_20_gb300/csrc/decode_gated.cu"),
@@ -337,7 +337,7 @@ def run_ours(args, rank, world, local_rank):
               "workload": wd.name, "l2": "flushed (256 MiB write) before every launch",
               "roofline": {"bound": "hbm", "achieved": dbytes / (dms * 1e-3) / 1e9, "peak": peaks["hbm"],
                            "unit": "GB/s", "frac": dbytes / (dms * 1e-3) / 1e9 / peaks["hbm"],
-                           "traffic": recorded_traffic("gdn_decode_kernel"), "kernel": "gdn_decode_kernel",
+                           "traffic": recorded_traffic("gdn_decode_stream_kernel"), "kernel": "gdn_decode_stream_kernel",
                            "algorithmic_bytes_per_launch": dbytes}}
     del xd, dstate, dout
 
@@ -403,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
              "l2": "flushed (256 MiB write) before every launch",
              "roofline": {"bound": "hbm", "achieved": gb / (gms * 1e-3) / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
                           "frac": gb / (gms * 1e-3) / 1e9 / peaks["hbm"],
-                          "traffic": recorded_traffic("gdn_decode_gated_kernel"), "kernel": "gdn_decode_gated_kernel",
+                          "traffic": recorded_traffic("gdn_decode_gated_stream_kernel"), "kernel": "gdn_decode_gated_stream_kernel",
                           "algorithmic_bytes_per_launch": gb}}
     del xg, gout
 
@@ -437,7 +437,7 @@ def run_ours(args, rank, world, local_rank):
              "l2": "flushed (256 MiB write) before every call",
              "roofline": {"bound": "hbm", "achieved": bb / (bms * 1e-3) / 1e9, "peak": peaks["hbm"], "unit": "GB/s",
                           "frac": bb / (bms * 1e-3) / 1e9 / peaks["hbm"], "traffic": recorded_traffic("decode_block"),
-                          "kernel": "inproj_gemm_kernel + gdn_decode_gated_kernel",
+                          "kernel": "inproj_gemm_kernel + gdn_decode_gated_stream_kernel",
                           "algorithmic_bytes_per_call": bb}}
     del xb, bws, bout, flush
 
