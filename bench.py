@@ -91,6 +91,13 @@ def block_bytes(w) -> int:
             w.C * w.K * 4 + 2 * w.Hv * 4 + w.Dv * 4 + w.B * vd * 2)
 
 
+def norm_bytes(w) -> int:
+    """Algorithmic bytes of the RMSNormGated pass over a prefill's output: the output
+    read and rewritten, z read, and norm_weight."""
+    e = 2 if w.dtype == "bf16" else 4
+    return 3 * w.B * w.Hv * w.S * w.Dv * e + w.Dv * 4
+
+
 def decode_bytes(w) -> int:
     e = 2 if w.dtype == "bf16" else 4
     return (2 * w.B * w.Hv * w.Dk * w.Dv * 4 + 2 * w.B * w.Hk * w.Dk * e + 2 * w.B * w.Hv * w.Dv * e
@@ -309,6 +316,35 @@ def run_ours(args, rank, world, local_rank):
                        "frac": pflops / avg_launch_s / 1e12 / peaks["bf16_sustained"],
                        "algorithmic_flops_per_launch": pflops}}
 
+    # ---------------- the gated prefill (the prefill, then RMSNormGated on its output), inputs > L2
+    gz = workloads.make_gate_inputs(w, device=dev)
+    gstate = x["state"].clone()
+    gout = torch.empty_like(out)
+
+    def gated_prefill_step():
+        gdn.prefill_gated(x["q"], x["k"], x["v"], x["g_log"], x["beta"], gz["z"], gz["norm_weight"], x["scale"],
+                          gstate, gout, stream=stream)
+
+    for _ in range(max(args.warmup, 3)):
+        gated_prefill_step()
+    torch.cuda.synchronize()
+    gev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(min(args.steps, 50))]
+    for a_, b_ in gev:
+        a_.record(stream)
+        gated_prefill_step()
+        b_.record(stream)
+    torch.cuda.synchronize()
+    gpms = statistics.median([a_.elapsed_time(b_) for a_, b_ in gev])
+    nbytes = norm_bytes(w)
+    prefill_gated = {"workload": w.name, "ms": gpms, "tokens_per_s": w.B * w.S / (gpms * 1e-3) * world,
+                     "kernels": 2, "norm_pass_ms": gpms - statistics.median(launch_ms),
+                     "norm_pass_roofline": {"bound": "hbm", "algorithmic_bytes_per_launch": nbytes,
+                                            "achieved": nbytes / ((gpms - statistics.median(launch_ms)) * 1e-3) / 1e9,
+                                            "peak": peaks["hbm"], "unit": "GB/s",
+                                            "note": "norm pass time = gated-prefill median minus prefill median"}}
+    prefill_gated["norm_pass_roofline"]["frac"] = prefill_gated["norm_pass_roofline"]["achieved"] / peaks["hbm"]
+    del gz, gstate, gout
+
     # ---------------- decode step, L2 flushed between launches
     wd = rank_workload(DECODE, rank)
     xd = workloads.make_inputs(wd, device=dev)
@@ -508,7 +544,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "Hk": w.Hk, "Hv": w.Hv, "S": w.S, "Dk": w.Dk, "Dv": w.Dv,
                    "parallelism": "independent sequences per rank" if world > 1 else "single gpu",
                    "l2": "inputs larger than L2 (%.0f MB per step)" % (pbytes / 1e6)},
-        "roofline": roof, "decode": decode, "decode_gated": gated, "decode_block": block, "conv1d": conv, "e2e": e2e, "clocks": clocks,
+        "roofline": roof, "prefill_gated": prefill_gated, "decode": decode, "decode_gated": gated, "decode_block": block, "conv1d": conv, "e2e": e2e, "clocks": clocks,
         "gpu_launches": args.steps * gdn.kernels_per_call(),
         "launch_ms": {"median": statistics.median(launch_ms), "min": min(launch_ms), "max": max(launch_ms)},
     }

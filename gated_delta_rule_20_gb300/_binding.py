@@ -31,7 +31,8 @@ GDN_FORCE_FFMA = 1 << 1
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
             "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
-            "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block")
+            "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block", "gdn_rmsnorm_gated",
+            "gdn_prefill_gated")
 
 
 class GdnDims(ctypes.Structure):
@@ -94,6 +95,11 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = [vp, fp, vp, vp, ctypes.POINTER(GdnConvDims), vp]
+        L.gdn_rmsnorm_gated.restype = ctypes.c_int
+        L.gdn_rmsnorm_gated.argtypes = [vp, vp, fp, vp, ctypes.c_int64, ctypes.c_int64, ctypes.c_int32, vp]
+        L.gdn_prefill_gated.restype = ctypes.c_int
+        L.gdn_prefill_gated.argtypes = [vp, vp, vp, fp, fp, vp, fp, ctypes.c_float, fp, vp, ctypes.POINTER(GdnDims),
+                                        vp]
         _lib = L
     return _lib
 
@@ -176,6 +182,60 @@ def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=Fal
     if out is None:
         out = torch.empty((B, Hv, S, Dv), dtype=q.dtype, device=q.device)
     return _call("gdn_prefill", q, k, v, g_log, beta, scale, state, out, zero, force_ffma, stream)
+
+
+def rmsnorm_gated(x, z, norm_weight, out=None, *, stream=None):
+    """RMSNormGated over the last dimension (``gdn_rmsnorm_gated``): x, z [..., D] in the compute
+    dtype, norm_weight [D] fp32; ``out`` may be ``x``.  Returns ``out``."""
+    torch = _torch()
+    if out is None:
+        out = torch.empty_like(x)
+    for nm, t in (("x", x), ("z", z), ("norm_weight", norm_weight), ("out", out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % nm)
+    if z.shape != x.shape or out.shape != x.shape or z.dtype != x.dtype or out.dtype != x.dtype:
+        raise ValueError("x, z and out must share shape and dtype")
+    if norm_weight.dtype != torch.float32 or norm_weight.shape != (x.shape[-1],):
+        raise ValueError("norm_weight must be float32 [D]")
+    D = x.shape[-1]
+    rows = x.numel() // D if D else 0
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        _check(lib().gdn_rmsnorm_gated(_ptr(x), _ptr(z), _ptr(norm_weight), _ptr(out), rows, D, _dtype_code(x),
+                                       ctypes.c_void_p(stream.cuda_stream)))
+    return out
+
+
+def prefill_gated(q, k, v, g_log, beta, z, norm_weight, scale, state=None, out=None, *, force_ffma=False,
+                  stream=None):
+    """``gdn_prefill_gated``: the prefill with RMSNormGated on its output, z [B,Hv,S,Dv] in the
+    compute dtype, norm_weight [Dv] fp32.  Returns ``(out, state)`` as ``prefill``."""
+    torch = _torch()
+    B, Hk, S, Dk = q.shape
+    Hv, Dv = v.shape[1], v.shape[3]
+    zero = state is None
+    if zero:
+        state = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
+    if out is None:
+        out = torch.empty((B, Hv, S, Dv), dtype=q.dtype, device=q.device)
+    for nm, t in (("q", q), ("k", k), ("v", v), ("g_log", g_log), ("beta", beta), ("z", z),
+                  ("norm_weight", norm_weight), ("state", state), ("out", out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % nm)
+    if z.dtype != q.dtype or tuple(z.shape) != (B, Hv, S, Dv):
+        raise ValueError("z must be [B,Hv,S,Dv] in the compute dtype")
+    if norm_weight.dtype != torch.float32 or tuple(norm_weight.shape) != (Dv,):
+        raise ValueError("norm_weight must be float32 [Dv]")
+    flags = (GDN_ZERO_INITIAL_STATE if zero else 0) | (GDN_FORCE_FFMA if force_ffma else 0)
+    dims = make_dims(B, Hk, Hv, S, Dk, Dv, _dtype_code(q), flags)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _check(lib().gdn_prefill_gated(_ptr(q), _ptr(k), _ptr(v), _ptr(g_log), _ptr(beta), _ptr(z),
+                                       _ptr(norm_weight), ctypes.c_float(scale), _ptr(state), _ptr(out),
+                                       ctypes.byref(dims), ctypes.c_void_p(stream.cuda_stream)))
+    return out, state
 
 
 def decode_step(q, k, v, g_log, beta, scale, state, out=None, *, stream=None):

@@ -21,7 +21,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libgdn.so")
 
-SOURCES = ["gdn_api.cu", "decode.cu", "prefill_ffma.cu", "prefill_tc.cu", "conv1d.cu", "decode_gated.cu", "block.cu"]
+SOURCES = ["gdn_api.cu", "decode.cu", "prefill_ffma.cu", "prefill_tc.cu", "conv1d.cu", "decode_gated.cu", "block.cu",
+           "rmsnorm_gated.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

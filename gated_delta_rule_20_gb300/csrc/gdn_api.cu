@@ -85,6 +85,13 @@ gdn_status empty_sequence(const Problem& p, cudaStream_t stream) {
 }
 
 }  // namespace
+
+gdn_status prefill_checked(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
+                           float* state, void* out, const gdn_dims* d) {
+    Problem p{};
+    return check(q, k, v, g_log, beta, state, out, d, false, &p);
+}
+
 }  // namespace gdn
 
 extern "C" {

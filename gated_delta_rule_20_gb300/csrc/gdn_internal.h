@@ -27,6 +27,10 @@ struct Problem {
 // else a gdn_status written by a kernel whose wait gave up).
 gdn_status status_word_for_current_device(int32_t** out);
 
+// The argument checks of gdn_prefill, without launching anything.
+gdn_status prefill_checked(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
+                           float* state, void* out, const gdn_dims* d);
+
 // Decode step (S == 1): one pass over the fp32 state.
 cudaError_t launch_decode(const Problem& p, cudaStream_t stream);
 

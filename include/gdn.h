@@ -248,6 +248,34 @@ gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, const void* W
                             float* state_inout, void* out, void* workspace, size_t workspace_bytes,
                             const gdn_block_dims* dims, gdn_stream_t stream);
 
+/*
+ * gdn_rmsnorm_gated -- the RMSNormGated output epilogue ("GDN Block TKG Kernel
+ * API Reference": Returns, "RMSNormGated decode output"; norm_weight, the
+ * "RMSNormGated weight") over `rows` rows of D elements:
+ *     out[r, :] = x[r, :] / sqrt(mean(x[r, :]^2) + GDN_RMSNORM_EPS) * norm_weight * silu(z[r, :])
+ *   x, z, out   [rows, D] in `dtype` (GDN_BF16 or GDN_F32), element-aligned;
+ *               out may be x (in place)
+ *   norm_weight [D] fp32
+ * rows >= 0, 1 <= D <= 4096.  One launch on `stream`.
+ */
+gdn_status gdn_rmsnorm_gated(const void* x, const void* z, const float* norm_weight, void* out, int64_t rows,
+                             int64_t D, int32_t dtype, gdn_stream_t stream);
+
+/*
+ * gdn_prefill_gated -- gdn_prefill followed by gdn_rmsnorm_gated on its output,
+ * per token and value head over Dv (the decode block's RMSNormGated applied to
+ * every token of a prefill):
+ *   z           [B, Hv, S, Dv] in the compute dtype (head-major, like out)
+ *   norm_weight [Dv] fp32
+ *   the other arguments as gdn_prefill; out receives the gated output.
+ * Every check of both steps runs before the first launch.  Launches the
+ * prefill's kernel, then one normalisation pass that reads the output and z
+ * and rewrites the output in place.
+ */
+gdn_status gdn_prefill_gated(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
+                             const void* z, const float* norm_weight, float scale, float* state_inout, void* out,
+                             const gdn_dims* dims, gdn_stream_t stream);
+
 /* Device workspace gdn_prefill needs for these dims: always 0 (every kernel
  * keeps its intermediates on chip). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);

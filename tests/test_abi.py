@@ -168,3 +168,23 @@ def test_decode_block_argument_checks(L):
     need = L.gdn_decode_block_workspace_bytes(ctypes.byref(D(B=64, H=2048, Hk=16, Hv=32, Dk=128, Dv=128)))
     assert need >= 64 * (4096 + 64) * 2   # z, a, b in bf16
     assert L.gdn_decode_block_workspace_bytes(ctypes.byref(D(dtype=gdn.GDN_F32))) == 0
+
+
+def test_rmsnorm_and_gated_prefill_argument_checks(L):
+    """Host-side checks of gdn_rmsnorm_gated and gdn_prefill_gated (no GPU needed)."""
+    p = ctypes.c_void_p(0x1000)
+    norm = lambda x=p, rows=4, D=128, dtype=gdn.GDN_BF16, w=p: L.gdn_rmsnorm_gated(x, p, w, p, rows, D, dtype, None)
+    assert norm(rows=0) == gdn.GDN_OK
+    assert norm(dtype=5) == gdn.GDN_ERR_UNSUPPORTED
+    assert norm(D=0) == gdn.GDN_ERR_DIMS and norm(rows=-1) == gdn.GDN_ERR_DIMS
+    assert norm(x=None) == gdn.GDN_ERR_NULL
+    assert norm(x=ctypes.c_void_p(0x1001)) == gdn.GDN_ERR_ALIGN          # a bf16 row off by a byte
+    assert norm(w=ctypes.c_void_p(0x1002)) == gdn.GDN_ERR_ALIGN          # fp32 weights
+    d = lambda **kw: gdn.make_dims(kw.get("B", 2), 2, 4, kw.get("S", 64), 128, kw.get("Dv", 128), gdn.GDN_BF16)
+    gp = lambda dims, z=p, w=p: L.gdn_prefill_gated(p, p, p, p, p, z, w, ctypes.c_float(1.0), p, p,
+                                                    ctypes.byref(dims) if dims is not None else None, None)
+    assert gp(None) == gdn.GDN_ERR_NULL
+    assert gp(d(), z=None) == gdn.GDN_ERR_NULL                             # checked before the prefill launches
+    assert gp(d(), w=ctypes.c_void_p(0x1002)) == gdn.GDN_ERR_ALIGN
+    assert gp(d(Dv=129)) == gdn.GDN_ERR_DIMS
+    assert gp(d(B=0)) == gdn.GDN_OK

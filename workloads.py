@@ -226,6 +226,18 @@ def make_gated_inputs(w: GatedWorkload, device="cpu"):
     return out
 
 
+# ------------------------------------------------------------------ the gated prefill
+# The prefill's inputs (make_inputs) plus the RMSNormGated inputs of every token, drawn
+# from their own generator (seed + 500): z ~ N(0, 1) [B, Hv, S, Dv] in the compute dtype,
+# norm_weight = 1 + 0.1 N(0, 1) [Dv] fp32.
+
+def make_gate_inputs(w: Workload, device="cpu"):
+    gen = torch.Generator(device="cpu").manual_seed(w.seed + 500)
+    z = torch.randn((w.B, w.Hv, w.S, w.Dv), generator=gen, dtype=torch.float32).to(w.torch_dtype)
+    norm_weight = 1.0 + 0.1 * torch.randn((w.Dv,), generator=gen, dtype=torch.float32)
+    return dict(z=z.to(device), norm_weight=norm_weight.to(device))
+
+
 # ------------------------------------------------------------------ the decode block
 # The whole decode block without its output projection: the token's hidden state,
 # the four input projections, the conv1d and the gated step.  Hidden size H = 2048.
