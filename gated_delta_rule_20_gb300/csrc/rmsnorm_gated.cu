@@ -31,7 +31,8 @@ __device__ __forceinline__ float warp_sum(float x) {
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     return x;
 }
-__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
+// silu(z) = z / (1 + e^-z) with the fast exponential and division (a few ulp)
+__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 template <typename T>
 __device__ __forceinline__ float to_f32(T x);
