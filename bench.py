@@ -39,6 +39,7 @@ KERNEL_SOURCES = {
     "conv1d_decode_k4_kernel": "gated_delta_rule_20_gb300/csrc/conv1d.cu",
     "gdn_decode_gated_stream_kernel": "gated_delta_rule_20_gb300/csrc/decode_gated.cu",
     "inproj_gemm_kernel": "gated_delta_rule_20_gb300/csrc/block.cu",
+    "rmsnorm_gated_d128_kernel": "gated_delta_rule_20_gb300/csrc/rmsnorm_gated.cu",
     # the two kernels of one decode-block call; the sha covers both files, in this order
     "decode_block": ("gated_delta_rule_20_gb300/csrc/block.cu", "gated_delta_rule_20_gb300/csrc/decode_gated.cu"),
 }
@@ -341,6 +342,8 @@ def run_ours(args, rank, world, local_rank):
                      "norm_pass_roofline": {"bound": "hbm", "algorithmic_bytes_per_launch": nbytes,
                                             "achieved": nbytes / ((gpms - statistics.median(launch_ms)) * 1e-3) / 1e9,
                                             "peak": peaks["hbm"], "unit": "GB/s",
+                                            "traffic": recorded_traffic("rmsnorm_gated_d128_kernel"),
+                                            "kernel": "rmsnorm_gated_d128_kernel",
                                             "note": "norm pass time = gated-prefill median minus prefill median"}}
     prefill_gated["norm_pass_roofline"]["frac"] = prefill_gated["norm_pass_roofline"]["achieved"] / peaks["hbm"]
     del gz, gstate, gout
