@@ -19,6 +19,7 @@
 #include <cstdint>
 
 #include "gdn.h"
+#include "gdn_device.cuh"
 
 namespace gdn {
 namespace {
@@ -26,30 +27,8 @@ namespace {
 constexpr int kMaxTaps = 8;
 constexpr int kThreadsPerBlock = 256;
 
-// silu(z) = z / (1 + e^-z), with the fast exponential and division (a few ulp of
-// fp32, far inside the outputs' bf16 rounding and the fp32 tolerance).
-__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+__device__ __forceinline__ float silu(float z) { return silu_fast(z); }
 
-template <typename T>
-__device__ __forceinline__ float to_f32(T v);
-template <>
-__device__ __forceinline__ float to_f32<float>(float v) {
-    return v;
-}
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 v) {
-    return __bfloat162float(v);
-}
-template <typename T>
-__device__ __forceinline__ T from_f32(float v);
-template <>
-__device__ __forceinline__ float from_f32<float>(float v) {
-    return v;
-}
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
-    return __float2bfloat16_rn(v);
-}
 
 __device__ __forceinline__ void unpack8(uint4 u, float* f) {
     const uint32_t w[4] = {u.x, u.y, u.z, u.w};

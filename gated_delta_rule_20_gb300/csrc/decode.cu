@@ -24,6 +24,7 @@
 #include <mutex>
 
 #include "gdn_internal.h"
+#include "gdn_device.cuh"
 #include "sm100_ptx.cuh"
 
 namespace gdn {
@@ -33,20 +34,6 @@ constexpr int kCols = 64;         // state columns per CTA
 constexpr int kThreads = 128;     // 16 column groups x 8 row groups
 constexpr int kRowGroups = 8;
 constexpr int kMaxRowsPerThread = 128 / kRowGroups;
-
-template <typename T>
-__device__ __forceinline__ float to_f32(T x);
-template <>
-__device__ __forceinline__ float to_f32<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) { return __bfloat162float(x); }
-
-template <typename T>
-__device__ __forceinline__ T from_f32(float x);
-template <>
-__device__ __forceinline__ float from_f32<float>(float x) { return x; }
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) { return __float2bfloat16_rn(x); }
 
 template <typename T, bool kVec>
 __global__ void __launch_bounds__(kThreads, 4) gdn_decode_kernel(const T* __restrict__ q, const T* __restrict__ k,

@@ -22,6 +22,7 @@
 #include <mutex>
 
 #include "gdn_internal.h"
+#include "gdn_device.cuh"
 #include "sm100_ptx.cuh"
 
 namespace gdn {
@@ -34,32 +35,7 @@ constexpr int kMaxRows = 128 / kRowGroups;
 constexpr float kEpsL2 = 1e-6f;
 constexpr float kEpsRms = 1e-6f;
 
-template <typename T>
-__device__ __forceinline__ float to_f32(T x);
-template <>
-__device__ __forceinline__ float to_f32<float>(float x) {
-    return x;
-}
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-    return __bfloat162float(x);
-}
-template <typename T>
-__device__ __forceinline__ T from_f32(float x);
-template <>
-__device__ __forceinline__ float from_f32<float>(float x) {
-    return x;
-}
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
-    return __float2bfloat16_rn(x);
-}
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
 __device__ __forceinline__ float softplus(float x) { return x > 20.f ? x : log1pf(expf(x)); }
 
 struct GatedArgs {
@@ -90,7 +66,6 @@ struct GatedArgs {
 // conv1d decode output from the window (K == 4 as one 8-byte word / any K).
 enum InputMode { kDirect = 0, kConv4 = 1, kConvAny = 2 };
 
-__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.f + __expf(-z)); }
 
 // conv1d decode output of one channel from its shifted window (4 bf16, oldest first, in one
 // 8-byte word) and its taps, rounded to bf16 as the stand-alone conv step stores it

@@ -18,6 +18,7 @@
 #include <cstdint>
 
 #include "gdn_internal.h"
+#include "gdn_device.cuh"
 
 namespace gdn {
 namespace {
@@ -26,34 +27,8 @@ constexpr int kRowsPerBlock = 8;  // scalar kernel: one warp per row, 256 thread
 constexpr int kRowIters = 4;      // D = 128 kernel: row groups per warp
 constexpr float kEps = GDN_RMSNORM_EPS;
 
-__device__ __forceinline__ float warp_sum(float x) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    return x;
-}
-// silu(z) = z / (1 + e^-z) with the fast exponential and division (a few ulp)
-__device__ __forceinline__ float silu(float z) { return __fdividef(z, 1.f + __expf(-z)); }
+__device__ __forceinline__ float silu(float z) { return silu_fast(z); }
 
-template <typename T>
-__device__ __forceinline__ float to_f32(T x);
-template <>
-__device__ __forceinline__ float to_f32<float>(float x) {
-    return x;
-}
-template <>
-__device__ __forceinline__ float to_f32<__nv_bfloat16>(__nv_bfloat16 x) {
-    return __bfloat162float(x);
-}
-template <typename T>
-__device__ __forceinline__ T from_f32(float x);
-template <>
-__device__ __forceinline__ float from_f32<float>(float x) {
-    return x;
-}
-template <>
-__device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float x) {
-    return __float2bfloat16_rn(x);
-}
 
 // D = 128, 16-byte aligned: a row is kLanes lanes x 8 (bf16) or 4 (fp32) elements; a warp
 // holds 32 / kLanes rows at a time and kRowIters such groups.
