@@ -115,15 +115,25 @@ def load_peaks():
     return dict(hbm=6800.0, bf16=1900.0, bf16_sustained=1700.0, source="fallback")
 
 
+def code_sha(paths) -> str:
+    """sha256[:16] of the sources' code with comments and blank lines removed, so that a
+    comment edit does not invalidate a recorded capture but any code change does."""
+    import hashlib
+    import re
+    text = b"".join(open(os.path.join(ROOT, f), "rb").read() for f in paths).decode()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    lines = [ln.rstrip() for ln in text.split("\n") if ln.strip()]
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()[:16]
+
+
 def recorded_traffic(kernel: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current source of the kernel (else None)."""
-    import hashlib
+    the current code of the kernel (else None)."""
     if not os.path.exists(PROFILE_TRAFFIC):
         return None
     srcs = KERNEL_SOURCES[kernel]
-    srcs = (srcs,) if isinstance(srcs, str) else srcs
-    sha = hashlib.sha256(b"".join(open(os.path.join(ROOT, f), "rb").read() for f in srcs)).hexdigest()[:16]
+    sha = code_sha((srcs,) if isinstance(srcs, str) else srcs)
     for line in open(PROFILE_TRAFFIC):
         parts = line.strip().strip("|").split("|")
         parts = [p.strip() for p in parts]

@@ -13,12 +13,15 @@
 // kernel is built around one coalesced pass: every fp32 state element is loaded
 // once with a 128-bit load into registers, reduced, updated and stored once.
 //
-// Grid: (B * Hv, ceil(Dv / 64)).  A CTA owns one 64-column slice of one head's
-// state (columns evolve independently: column c of S' depends only on column c
-// of S).  128 threads = 16 column groups of 4 floats x 8 row groups; thread
-// (rg, cg) holds rows rg, rg + 8, ... of its 4 columns.  A warp therefore reads
-// two full 256-byte row segments per load instruction.  Four CTAs share an SM
-// (128 registers per thread), so that more state loads are in flight.
+// Dk = Dv = 128 runs gdn_decode_stream_kernel (below): persistent CTAs that
+// bulk-copy the next head's state into shared memory while they compute the
+// current one.  Other head dims run gdn_decode_kernel.  Grid: (B * Hv,
+// ceil(Dv / 64)).  A CTA owns one 64-column slice of one head's state (columns
+// evolve independently: column c of S' depends only on column c of S).  128
+// threads = 16 column groups of 4 floats x 8 row groups; thread (rg, cg) holds
+// rows rg, rg + 8, ... of its 4 columns.  A warp therefore reads two full
+// 256-byte row segments per load instruction.  Four CTAs share an SM (128
+// registers per thread), so that more state loads are in flight.
 #include <cuda_bf16.h>
 
 #include <mutex>

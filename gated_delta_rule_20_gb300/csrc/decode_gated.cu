@@ -11,10 +11,14 @@
 //     o  = scale (e^g p_q + d (k^ . q^)),   S' = e^g S + k^ d^T   (in place)
 //     y  = o / sqrt(mean_Dv(o^2) + eps_rms) * norm_weight * silu(z)
 //
-// One CTA per (batch, value head) covers all Dv <= 128 columns, because the
-// RMS norm runs over the whole head: 256 threads = 32 column groups of 4 floats
-// x 8 row groups; a warp reads one full 512-byte state row segment per load.
-// Every fp32 state element is read once and written once.
+// A CTA of 256 threads covers all Dv <= 128 columns of a head, because the RMS
+// norm runs over the whole head: 32 column groups of 4 floats x 8 row groups.
+// Every fp32 state element is read once and written once.  At Dk = Dv = 128
+// with 16-byte aligned rows, persistent CTAs (two per SM) stream the heads
+// through shared memory (gdn_decode_gated_stream_kernel); other shapes run one
+// CTA per head (gdn_decode_gated_kernel).  Both share the per-head math
+// (gated_head).  In its conv mode (the decode block) the kernel computes q, k, v
+// from the shifted conv windows instead of reading them.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
