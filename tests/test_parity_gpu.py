@@ -10,6 +10,7 @@ import pytest
 import torch
 
 import gated_delta_rule_20_gb300 as gdn
+import oracle  # noqa: E402
 import workloads
 from gpu_util import check, oracle_for, rel_l2, run_prefill, to64
 
@@ -55,6 +56,21 @@ def test_decode_full_workload():
     ro, rs = oracle_for(x)
     eo, es = check(out, st, ro, rs, True, "decode full")
     assert eo < 5e-3 and es < 1e-5  # out rounds once to bf16; the state stays fp32
+
+
+def test_decode_zero_initial_state_full_size():
+    """GDN_ZERO_INITIAL_STATE on the decode step (through the C ABI), at the full size so that
+    every CTA of the streaming kernel walks several heads: equals the oracle from a zero state,
+    and the state buffer's previous contents (NaN here) are never read."""
+    from gated_delta_rule_20_gb300 import _binding as B
+    w = workloads.DECODE_STEP
+    x = workloads.make_inputs(w, device=DEV)
+    st = torch.full_like(x["state"], float("nan"))
+    out = torch.empty_like(x["v"])
+    B._call("gdn_decode_step", x["q"], x["k"], x["v"], x["g_log"], x["beta"], x["scale"], st, out, True, False, None)
+    torch.cuda.synchronize()
+    ro, rs = oracle.recurrence(x["q"], x["k"], x["v"], x["g_log"], x["beta"], x["scale"], None)
+    check(out, st, ro, rs, True, "decode zero start")
 
 
 def test_decode_equals_prefill_at_one_token():
