@@ -268,6 +268,26 @@ def time_oracle(w, n_seq: int, sample=None):
 
 
 # ------------------------------------------------------------------ our implementation
+def sustained(torch, stream, calls, n_steps, nbytes, peak):
+    """Back-to-back launches cycling through ``calls`` (one per input set, each set holding its
+    own state, so that three sets are larger than L2 and no step finds its state in L2); one
+    event pair around the whole loop.  The steady-state rate of a serving loop: launch latency
+    overlaps the previous step, and no L2 flush runs (nor leaves dirty lines) in between."""
+    for i in range(len(calls)):
+        calls[i]()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(n_steps):
+        calls[i % len(calls)]()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / n_steps
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    return {"ms": ms, "value": gbs, "unit": "GB/s", "frac": gbs / peak, "steps": n_steps, "input_sets": len(calls),
+            "method": "back-to-back launches over %d input sets, each with its own state (> L2 together)" % len(calls)}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import torch.distributed as dist
@@ -388,7 +408,12 @@ def run_ours(args, rank, world, local_rank):
                            "unit": "GB/s", "frac": dbytes / (dms * 1e-3) / 1e9 / peaks["hbm"],
                            "traffic": recorded_traffic("gdn_decode_stream_kernel"), "kernel": "gdn_decode_stream_kernel",
                            "algorithmic_bytes_per_launch": dbytes}}
-    del xd, dstate, dout
+    sets = [dict(xd, state=xd["state"].clone()) for _ in range(3)]
+    decode["sustained"] = sustained(
+        torch, stream, [lambda st=st_["state"]: gdn.decode_step(xd["q"], xd["k"], xd["v"], xd["g_log"], xd["beta"],
+                                                                  xd["scale"], st, dout, stream=stream) for st_ in sets],
+        max(30, min(args.steps, 300)), dbytes, peaks["hbm"])
+    del xd, dstate, dout, sets
 
     # ---------------- conv1d in front of the recurrence: prefill (input > L2) and decode (L2 flushed)
     conv = {}
@@ -454,7 +479,13 @@ def run_ours(args, rank, world, local_rank):
                           "frac": gb / (gms * 1e-3) / 1e9 / peaks["hbm"],
                           "traffic": recorded_traffic("gdn_decode_gated_stream_kernel"), "kernel": "gdn_decode_gated_stream_kernel",
                           "algorithmic_bytes_per_launch": gb}}
-    del xg, gout
+    gsets = [xg["state"].clone() for _ in range(3)]
+    gated["sustained"] = sustained(
+        torch, stream, [lambda st=st_: gdn.decode_gated(xg["qkv"], xg["z"], xg["a"], xg["b"], xg["A_log"], xg["dt_bias"],
+                                                         xg["norm_weight"], xg["scale"], st, wg.Hk, wg.Hv, wg.Dk, wg.Dv,
+                                                         out=gout, stream=stream) for st_ in gsets],
+        max(30, min(args.steps, 300)), gb, peaks["hbm"])
+    del xg, gout, gsets
 
     # ---------------- the decode block (in_proj GEMM with the conv window shift, then the gated step
     #                  with the conv output), L2 flushed
@@ -488,7 +519,15 @@ def run_ours(args, rank, world, local_rank):
                           "frac": bb / (bms * 1e-3) / 1e9 / peaks["hbm"], "traffic": recorded_traffic("decode_block"),
                           "kernel": "inproj_gemm_kernel + gdn_decode_gated_stream_kernel",
                           "algorithmic_bytes_per_call": bb}}
-    del xb, bws, bout, flush
+    bsets = [workloads.make_block_inputs(wb.with_(seed=wb.seed + 1 + i), device=dev) for i in range(3)]
+    block["sustained"] = sustained(
+        torch, stream, [lambda t=t: gdn.decode_block(t["hidden"], t["W_qkv"], t["W_z"], t["W_a"], t["W_b"],
+                                                     t["conv_weight"], t["conv_state"], t["A_log"], t["dt_bias"],
+                                                     t["norm_weight"], t["state"], wb.Hk, wb.Hv, wb.Dk, wb.Dv,
+                                                     out=bout, workspace=bws, stream=stream) for t in bsets],
+        max(30, min(args.steps, 300)), bb, peaks["hbm"])
+    block["sustained"]["method"] = "back-to-back calls over 3 input sets, each with its own weights and states"
+    del xb, bws, bout, flush, bsets
 
     # ---------------- end to end through the public API from pinned host buffers
     # Every step copies its inputs and initial state from pinned host memory, runs gdn_prefill
