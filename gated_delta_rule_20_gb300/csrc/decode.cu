@@ -191,7 +191,7 @@ __global__ void __launch_bounds__(kSThreads, 2) gdn_decode_stream_kernel(Problem
     auto head_of = [&](int l) { return (int)blockIdx.x + l * (int)gridDim.x; };
     auto load_state = [&](int bh) {
         ptx::mbar_arrive_expect_tx(&sm.full, kSStateBytes);
-        ptx::bulk_load(sm.state, p.state + (size_t)bh * kSD * kSD, kSStateBytes, &sm.full);
+        ptx::bulk_load_evict_first(sm.state, p.state + (size_t)bh * kSD * kSD, kSStateBytes, &sm.full);
     };
     // q, k (key head h / (Hv / Hk)) and v rows of head bh: 3 x 128 elements
     auto load_inputs = [&](int bh) {

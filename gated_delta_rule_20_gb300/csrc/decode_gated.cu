@@ -352,7 +352,7 @@ __global__ void __launch_bounds__(kThreads, 2) gdn_decode_gated_stream_kernel(Ga
     const int cg = tid & (kColGroups - 1), rg = tid >> 5, c0 = cg * 4;
     auto load_state = [&](int bh) {
         ptx::mbar_arrive_expect_tx(&sm.full, kStreamStateBytes);
-        ptx::bulk_load(sm.state, p.state + (long long)bh * kSD * kSD, kStreamStateBytes, &sm.full);
+        ptx::bulk_load_evict_first(sm.state, p.state + (long long)bh * kSD * kSD, kStreamStateBytes, &sm.full);
     };
     __shared__ int s_next;
     if (tid == 0) {
