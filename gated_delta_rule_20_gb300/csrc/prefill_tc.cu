@@ -27,18 +27,19 @@
 //     R_D[b] right half += Delta^T P^T                          -> O^T / scale
 //     R_S   += (Delta^T diag(exp(G_C - G))) K                   -> state increment, S^T layout
 //
-// Roles (one CTA per (batch, value head), 384 threads):
-//   prep warps (0-7)  -- per chunk: decay scan (one chunk ahead), the Gram
-//       product, A and P, Q -> Q' in place, the triangular solve, T diag(beta)
-//       and T diag(beta gamma) in bf16, and the U/W product, whose completion
-//       the chain waits for.  Warp w reads TMEM lanes 32 (w % 4) .. + 31 and,
-//       for 64-column products, columns 32 (w / 4) .. + 31.
-//   chain warps (8-11) -- the serial part, thread i on TMEM lane i: -W over V,
-//       Delta, the state carry (fp32 S^T in TMEM, scaled by gamma_C when its
-//       bf16 copy is taken and incremented by the tensor core), the output and
-//       its TMA store.  Once the products of chunk c have completed, the chain
-//       reloads that chunk's input stage with chunk c + 3 (TMA) and prefetches
-//       chunk c + 4 into L2.
+// Roles (one CTA per (batch, value head), 512 threads):
+//   prep warps (0-7)  -- per chunk, one chunk ahead of the chain: the decay
+//       scan, A and P from the Gram product, Q -> Q' in place, the triangular
+//       solve into T diag(beta) and T diag(beta gamma) in bf16; one prep thread
+//       issues the next chunk's Gram product.  Warp w reads TMEM lanes
+//       32 (w % 4) .. + 31 and, for 64-column products, columns 32 (w / 4) .. + 31.
+//   chain warps (8-11) -- the serial part, thread i on TMEM lane i: the U/W
+//       product, Delta, the state carry (fp32 S^T in TMEM, scaled by gamma_C when
+//       its bf16 copy is taken and incremented by the tensor core).
+//   helper warps (12-15) -- off the serial path: -W over V, the output product
+//       O^T += Delta^T P^T, the output tile and its TMA store, and the input
+//       loads: a chunk's stage is reloaded with chunk c + 3 once its last
+//       product has read it, and chunk c + 4 is prefetched into L2.
 //
 // Triangular solve: (I + A)^-1 for the 64x64 strictly lower A, blocked in
 // 16x16: diagonal blocks by forward substitution in fp32, off-diagonal blocks
@@ -105,7 +106,8 @@ constexpr uint32_t OFF_SMALL = OFF_OUT + 16384;
 // raw decay inputs (log-decay, beta) [2][2][64], slot c % 2, fetched asynchronously
 constexpr uint32_t SM_G = 0, SM_GAM = 128, SM_BET = 256, SM_EC = 384, SM_GC = 640, SM_GB = 704;
 constexpr uint32_t OFF_BAR = OFF_SMALL + 4096;
-constexpr uint32_t SMEM_USED = OFF_BAR + 128;
+constexpr uint32_t BARS_BYTES = 256;  // struct Bars (asserted below)
+constexpr uint32_t SMEM_USED = OFF_BAR + BARS_BYTES;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;
 static_assert(OFF_T12 % 1024 == 0 && OFF_OUT % 1024 == 0, "tile alignment");
 static_assert(SMEM_ALLOC <= 232448, "shared memory budget");
@@ -196,6 +198,7 @@ struct Bars {
     uint32_t tmem_base;
     int abort;
 };
+static_assert(sizeof(Bars) <= BARS_BYTES, "barrier block");
 
 // ---------------------------------------------------------------- solve
 // Warp-level tf32 fragments (m16n8k8) of fp32 matrices in shared memory.  The
