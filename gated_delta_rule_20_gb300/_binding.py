@@ -27,6 +27,7 @@ GDN_BF16 = 1
 
 GDN_ZERO_INITIAL_STATE = 1 << 0
 GDN_FORCE_FFMA = 1 << 1
+GDN_SINGLE_PASS = 1 << 2
 
 # Every symbol include/gdn.h declares.
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
@@ -135,7 +136,7 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, force_ffma, stream):
+def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, force_ffma, stream, single_pass=False):
     torch = _torch()
     for nm, t in (("q", q), ("k", k), ("v", v), ("g_log", g_log), ("beta", beta), ("state", state), ("out", out)):
         if not t.is_cuda:
@@ -155,7 +156,8 @@ def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, for
             tuple(g_log.shape) != (B, Hv, S) or tuple(beta.shape) != (B, Hv, S) or \
             tuple(state.shape) != (B, Hv, Dk, Dv) or tuple(out.shape) != (B, Hv, S, Dv):
         raise ValueError("inconsistent shapes")
-    flags = (GDN_ZERO_INITIAL_STATE if zero_initial_state else 0) | (GDN_FORCE_FFMA if force_ffma else 0)
+    flags = (GDN_ZERO_INITIAL_STATE if zero_initial_state else 0) | (GDN_FORCE_FFMA if force_ffma else 0) | \
+        (GDN_SINGLE_PASS if single_pass else 0)
     dims = make_dims(B, Hk, Hv, S, Dk, Dv, dt, flags)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
@@ -166,12 +168,13 @@ def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, for
     return out, state
 
 
-def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=False, stream=None):
+def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=False, single_pass=False, stream=None):
     """Chunked prefill (``gdn_prefill``).
 
     ``state`` [B,Hv,Dk,Dv] fp32 is updated in place and returned; ``None`` means
     the zero-start form (a new zero-initialised tensor receives the final
-    state).  Returns ``(out, state)``.
+    state).  ``single_pass`` sets ``GDN_SINGLE_PASS`` (no split into segments).
+    Returns ``(out, state)``.
     """
     torch = _torch()
     B, Hk, S, Dk = q.shape
@@ -181,7 +184,7 @@ def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=Fal
         state = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
     if out is None:
         out = torch.empty((B, Hv, S, Dv), dtype=q.dtype, device=q.device)
-    return _call("gdn_prefill", q, k, v, g_log, beta, scale, state, out, zero, force_ffma, stream)
+    return _call("gdn_prefill", q, k, v, g_log, beta, scale, state, out, zero, force_ffma, stream, single_pass)
 
 
 def rmsnorm_gated(x, z, norm_weight, out=None, *, stream=None):

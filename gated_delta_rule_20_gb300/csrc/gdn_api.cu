@@ -39,7 +39,7 @@ namespace {
 
 bool misaligned(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) != 0; }
 
-constexpr uint32_t kKnownFlags = GDN_ZERO_INITIAL_STATE | GDN_FORCE_FFMA;
+constexpr uint32_t kKnownFlags = GDN_ZERO_INITIAL_STATE | GDN_FORCE_FFMA | GDN_SINGLE_PASS;
 
 gdn_status check(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
                  float* state, void* out, const gdn_dims* d, bool decode, Problem* p) {
@@ -73,6 +73,7 @@ gdn_status check(const void* q, const void* k, const void* v, const float* g_log
     p->Dv = (int)d->Dv;
     p->bf16 = d->dtype == GDN_BF16;
     p->zero_init = (d->flags & GDN_ZERO_INITIAL_STATE) != 0;
+    p->single_pass = (d->flags & GDN_SINGLE_PASS) != 0;
     return GDN_OK;
 }
 

@@ -21,6 +21,7 @@ struct Problem {
     int B, Hk, Hv, S, Dk, Dv;
     bool bf16;       // compute dtype of q/k/v/out
     bool zero_init;  // GDN_ZERO_INITIAL_STATE
+    bool single_pass = false;  // GDN_SINGLE_PASS: never split a sequence into segments
 };
 
 // Device address of the current device's kernel-side status word (0 = fine,

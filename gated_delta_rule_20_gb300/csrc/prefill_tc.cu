@@ -265,8 +265,7 @@ __device__ __forceinline__ void solve_diag_block(float* M, int blk, int lane) {
 
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void load_chunk(uint8_t* st, uint64_t* bar, const CUtensorMap* tq, const CUtensorMap* tk,
-                                           const CUtensorMap* tv, int c, int bhk, int bh) {
-    const int t0 = c * kC;
+                                           const CUtensorMap* tv, int t0, int bhk, int bh) {
     mbar_arrive_expect_tx(bar, LOAD_BYTES);
     tma_load_3d(st + ST_K0, tk, bar, 0, t0, bhk);
     tma_load_3d(st + ST_Q0, tq, bar, 0, t0, bhk);
@@ -276,8 +275,7 @@ __device__ __forceinline__ void load_chunk(uint8_t* st, uint64_t* bar, const CUt
     tma_load_3d(st + ST_VW1, tv, bar, 64, t0, bh);
 }
 __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                                                  int c, int bhk, int bh) {
-    const int t0 = c * kC;
+                                                  int t0, int bhk, int bh) {
     tma_prefetch_l2_3d(tk, 0, t0, bhk);
     tma_prefetch_l2_3d(tk, 64, t0, bhk);
     tma_prefetch_l2_3d(tq, 0, t0, bhk);
@@ -287,11 +285,30 @@ __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const C
 }
 
 // ---------------------------------------------------------------- kernel
+// A launch processes up to kMaxRuns runs over the same heads: run r covers tokens
+// t0 .. t0 + len - 1 of every (batch, value head) sequence, CTA blockIdx.x = r * heads + head.
+// A plain prefill is one run over the whole sequence; a split one (host side, below) uses
+// runs over segments, some of them from a zero or identity start.
+struct PrefillRun {
+    const float* state_in;  // initial states, head h at state_in + h * in_stride; nullptr: zero
+    float* state_out;       // final states [heads, Dk, Dv]; may equal state_in
+    long long in_stride;    // Dk * Dv, or 0 (one start state for every head)
+    int t0, len;            // len >= 1; every run but a sequence's last covers whole chunks
+};
+constexpr int kMaxRuns = 16;
+struct PrefillRuns {
+    PrefillRun run[kMaxRuns];
+    int heads;
+};
+
+// kSplit = false: one run over whole sequences (runs.run[0], t0 = 0, len = S), the
+// instantiation a plain prefill launches; its code is that of a kernel without run tables.
+template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
                           const float* __restrict__ g_log, const float* __restrict__ beta,
-                          float* __restrict__ state, float scale, int Hk, int Hv, int S, int zero_init,
+                          const __grid_constant__ PrefillRuns runs, float scale, int Hk, int Hv, int S,
                           int32_t* __restrict__ status) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // Round up to 1024 bytes by indexing the shared array itself, so that every
@@ -311,11 +328,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
-    const int bh = blockIdx.x;
+    const int ri = kSplit ? blockIdx.x / runs.heads : 0;  // this CTA's run and (batch, value head)
+    const int bh = blockIdx.x - ri * runs.heads;
     const int b = bh / Hv;
     const int h = bh - b * Hv;
     const int bhk = b * Hk + h / (Hv / Hk);
-    const int n_chunks = (S + kC - 1) / kC;
+    const int tb = kSplit ? runs.run[ri].t0 : 0;  // the run covers tokens tb .. tb + len - 1
+    const int len = kSplit ? runs.run[ri].len : S;
+    const int n_chunks = (len + kC - 1) / kC;
 
     if (tid == 0) {
         for (int s = 0; s < kStages; ++s) {
@@ -384,9 +404,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         auto fetch_decays = [&](int cc, int i) {
             float* dst = sGB + 128 * (cc & 1);
             const int tn = cc * kC + i;
-            if (tn < S) {
-                cp_async_4(dst + i, g_log + (size_t)bh * S + tn);
-                cp_async_4(dst + 64 + i, beta + (size_t)bh * S + tn);
+            if (tn < len) {
+                cp_async_4(dst + i, g_log + (size_t)bh * S + tb + tn);
+                cp_async_4(dst + 64 + i, beta + (size_t)bh * S + tb + tn);
             } else {
                 dst[i] = 0.f;
                 dst[64 + i] = 0.f;
@@ -599,12 +619,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32u(trow + COL_SA + 32 * half, u);
         };
         {
-            const float* Sg = state + (size_t)bh * kD * kD;
+            // the initial state: the run's input (per head, or one matrix for all heads), or zero
+            const float* Sg = runs.run[ri].state_in + (size_t)bh * (kSplit ? runs.run[ri].in_stride : kD * kD);
+            const bool zero = runs.run[ri].state_in == nullptr;
 #pragma unroll 1
             for (int h64 = 0; h64 < 2; ++h64) {
                 float x[64];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) x[j] = zero_init ? 0.f : Sg[(size_t)(64 * h64 + j) * kD + ct];
+                for (int j = 0; j < 64; ++j) x[j] = zero ? 0.f : Sg[(size_t)(64 * h64 + j) * kD + ct];
                 tmem_st32(trow + COL_S + 64 * h64, *reinterpret_cast<const float(*)[32]>(x));
                 tmem_st32(trow + COL_S + 64 * h64 + 32, *reinterpret_cast<const float(*)[32]>(x + 32));
                 store_state_bf16(h64, x);
@@ -741,7 +763,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ok = !named_bar_any(BAR_CHAIN, kChain, !ok || *abort_flag != 0);
         if (ok && n_chunks > 0) {  // the final state
             tc_fence_after();
-            float* Sg = state + (size_t)bh * kD * kD;
+            float* Sg = runs.run[ri].state_out + (size_t)bh * kD * kD;
 #pragma unroll 1
             for (int c0 = 0; c0 < kD; c0 += 32) {
                 float x[32];
@@ -768,10 +790,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_v);
             tma_prefetch_desc(&tm_o);
             for (int c = 0; c < kStages && c < n_chunks; ++c) {
-                load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, c, bhk, bh);
+                load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, tb + c * kC, bhk, bh);
                 last_load = c;
             }
-            if (n_chunks > kStages) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, kStages, bhk, bh);
+            if (n_chunks > kStages) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, tb + kStages * kC, bhk, bh);
         }
         int issued3 = -1;  // last chunk whose output product was committed
         // Iteration c: the output of chunk c - 1 (its product, the tile, the store, the stage
@@ -801,9 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (named_bar_any(BAR_HELP, kHelp, fail)) break;
                 if (ht == 0 && p + kStages < n_chunks) {
                     // reload the stage with chunk p + kStages and prefetch the chunk after into L2
-                    load_chunk(sm + sp * STAGE_BYTES, &bars->full[sp], &tm_q, &tm_k, &tm_v, p + kStages, bhk, bh);
+                    load_chunk(sm + sp * STAGE_BYTES, &bars->full[sp], &tm_q, &tm_k, &tm_v, tb + (p + kStages) * kC,
+                               bhk, bh);
                     last_load = p + kStages;
-                    if (p + kStages + 1 < n_chunks) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, p + kStages + 1, bhk, bh);
+                    if (p + kStages + 1 < n_chunks)
+                        prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, tb + (p + kStages + 1) * kC, bhk, bh);
                 }
                 if (ht == 0) tma_store_wait_read0();  // the out tile of chunk p - 1 has been read
                 named_bar_sync(BAR_HELP, kHelp);
@@ -814,8 +838,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fence_proxy_async_smem();
                 named_bar_sync(BAR_HELP, kHelp);
                 if (ht == 0) {
-                    tma_store_3d(&tm_o, sm + OFF_OUT, 0, p * kC, bh);
-                    tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, p * kC, bh);
+                    tma_store_3d(&tm_o, sm + OFF_OUT, 0, tb + p * kC, bh);
+                    tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, tb + p * kC, bh);
                     tma_store_commit();
                 }
             }
@@ -888,6 +912,87 @@ bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// ---------------------------------------------------------------- split sequences
+// Start states of the later segments of a split prefill (blockIdx.x = head, blockIdx.y = a
+// slice of kCombCols state columns): for j = 1 .. n_maps, S_{j+1} = (R_j - X_j) S_j + X_j.
+// X_j is segment j's final state from a zero start and R_j the one from S0 = I; the chunk
+// recurrence is affine in its start state (S_end = M S0 + X), so R_j - X_j = M_j.  Each
+// state column evolves on its own, so the slices exchange nothing.  Plain fp32 FMAs.
+constexpr int kCombCols = 32;
+constexpr int kCombStride = kD + 1;  // padded rows of M: lane r of a warp reads bank (r + k) % 32
+constexpr size_t kCombSmem = (size_t)(kD * kCombStride + kD * kCombCols) * sizeof(float);
+
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ X, const float* __restrict__ R,
+                                                              float* __restrict__ Sst, int heads, int n_maps) {
+    extern __shared__ float csm[];
+    float* sM = csm;                     // [128][129]: R_j - X_j
+    float* sS = csm + kD * kCombStride;  // [128][32]: this slice of S_j
+    const int h = blockIdx.x, col0 = blockIdx.y * kCombCols, t = threadIdx.x;
+    const size_t hs = (size_t)kD * kD;
+    const float* S1 = Sst + (size_t)h * hs;
+    for (int i = t; i < kD * kCombCols; i += 256) sS[i] = S1[(size_t)(i / kCombCols) * kD + col0 + i % kCombCols];
+    const int r = t >> 1, c0 = (t & 1) * 16;  // this thread: row r, columns c0 .. c0 + 15 of the slice
+    for (int j = 1; j <= n_maps; ++j) {
+        const float* Xj = X + ((size_t)(j - 1) * heads + h) * hs;
+        const float* Rj = R + ((size_t)(j - 1) * heads + h) * hs;
+        for (int i = t; i < kD * kD / 4; i += 256) {
+            const float4 a = reinterpret_cast<const float4*>(Rj)[i];
+            const float4 x = reinterpret_cast<const float4*>(Xj)[i];
+            float* d = sM + (4 * i / kD) * kCombStride + 4 * i % kD;
+            d[0] = a.x - x.x;
+            d[1] = a.y - x.y;
+            d[2] = a.z - x.z;
+            d[3] = a.w - x.w;
+        }
+        __syncthreads();  // M_j and the S_j slice are complete
+        float acc[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+#pragma unroll 4
+        for (int k = 0; k < kD; ++k) {
+            const float m = sM[r * kCombStride + k];
+            const float4* srow = reinterpret_cast<const float4*>(sS + k * kCombCols + c0);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 v = srow[q];
+                acc[4 * q + 0] = fmaf(m, v.x, acc[4 * q + 0]);
+                acc[4 * q + 1] = fmaf(m, v.y, acc[4 * q + 1]);
+                acc[4 * q + 2] = fmaf(m, v.z, acc[4 * q + 2]);
+                acc[4 * q + 3] = fmaf(m, v.w, acc[4 * q + 3]);
+            }
+        }
+        __syncthreads();  // every thread has read M_j and S_j
+        float* Sn = Sst + ((size_t)j * heads + h) * hs;  // S_{j+1}
+#pragma unroll
+        for (int e = 0; e < 16; ++e) {
+            const size_t g = (size_t)r * kD + col0 + c0 + e;
+            const float v = acc[e] + Xj[g];
+            sS[r * kCombCols + c0 + e] = v;  // read in step j + 1 after its first barrier
+            Sn[g] = v;
+        }
+    }
+}
+
+// A Dk x Dv identity (one CTA per row).
+__global__ void identity_kernel(float* I) { I[blockIdx.x * kD + threadIdx.x] = blockIdx.x == threadIdx.x ? 1.f : 0.f; }
+
+// Segments for a prefill of `heads` sequences of n_chunks chunks on `sms` SMs (1: no split).
+// A split into P segments runs in two waves of about n_chunks / P chunks: first segment 0
+// from the real start state and, for each middle segment, one run from a zero start and one
+// from the identity (heads * (2P - 3) CTAs, one per SM); then segments 1 .. P - 1 from the
+// start states the combine kernel derives.  Worth it from P = 3, with segments of at least
+// 8 chunks; 2P - 3 runs must fit one launch.
+int split_segments(int heads, int n_chunks, int sms) {
+    if (heads * 3 > sms) return 1;
+    int P = (sms - heads) / (2 * heads) + 2;
+    P = P < (kMaxRuns + 3) / 2 ? P : (kMaxRuns + 3) / 2;
+    P = P < n_chunks / 8 ? P : n_chunks / 8;
+    if (P < 3) return 1;
+    const int L = (n_chunks + P - 1) / P;
+    P = (n_chunks + L - 1) / L;
+    return P >= 3 ? P : 1;
+}
+
 }  // namespace
 
 bool prefill_tc_supported(const Problem& p) { return p.bf16 && p.Dk == kD && p.Dv == kD; }
@@ -898,23 +1003,78 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
         !encode_bf16_3d(&tv, p.v, p.B * p.Hv, p.S, 64, true) ||
         !encode_bf16_3d(&to, p.out, p.B * p.Hv, p.S, 64, true))
         return GDN_ERR_CUDA;
-    // the shared-memory opt-in is set once per device
+    // the shared-memory opt-ins are set once per device; the SM count is read once
     static std::mutex mu;
     static bool configured[64] = {};
+    static int sm_count[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return GDN_ERR_CUDA;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (!configured[dev]) {
-            if (cudaFuncSetAttribute(gdn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)SMEM_ALLOC) != cudaSuccess)
+            if (cudaFuncSetAttribute(gdn_prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_ALLOC) != cudaSuccess ||
+                cudaFuncSetAttribute(gdn_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_ALLOC) != cudaSuccess ||
+                cudaFuncSetAttribute(prefill_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kCombSmem) != cudaSuccess ||
+                cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return GDN_ERR_CUDA;
             configured[dev] = true;
         }
     }
-    gdn_prefill_tc_kernel<<<p.B * p.Hv, kThreads, SMEM_ALLOC, stream>>>(
-        tq, tk, tv, to, p.g_log, p.beta, p.state, p.scale, p.Hk, p.Hv, p.S, p.zero_init ? 1 : 0, status_word);
-    return cudaGetLastError() == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+    const int heads = p.B * p.Hv;
+    auto launch = [&](const PrefillRuns& runs, int n_runs) {
+        if (n_runs == 1 && runs.run[0].t0 == 0 && runs.run[0].len == p.S)
+            gdn_prefill_tc_kernel<false><<<heads, kThreads, SMEM_ALLOC, stream>>>(
+                tq, tk, tv, to, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+        else
+            gdn_prefill_tc_kernel<true><<<heads * n_runs, kThreads, SMEM_ALLOC, stream>>>(
+                tq, tk, tv, to, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+        return cudaGetLastError() == cudaSuccess;
+    };
+    PrefillRuns runs{};
+    runs.heads = heads;
+    const int n_chunks = (p.S + kC - 1) / kC;
+    const int P = p.single_pass ? 1 : split_segments(heads, n_chunks, sm_count[dev]);
+    const size_t hs = (size_t)heads * kD * kD;  // floats in one state per head
+    const long long one = (long long)kD * kD;  // floats in one head's state
+    void* ws = nullptr;
+    // stream-ordered scratch: S_1 .. S_{P-1}, X_1 .. X_{P-2}, R_1 .. R_{P-2}, and one identity
+    if (P > 1 && cudaMallocAsync(&ws, ((size_t)(3 * P - 5) * hs + one) * sizeof(float), stream) != cudaSuccess) {
+        (void)cudaGetLastError();
+        ws = nullptr;
+    }
+    if (!ws) {  // one run over the whole sequence
+        runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S};
+        return launch(runs, 1) ? GDN_OK : GDN_ERR_CUDA;
+    }
+    float* Sst = static_cast<float*>(ws);
+    float* X = Sst + (size_t)(P - 1) * hs;
+    float* R = X + (size_t)(P - 2) * hs;
+    float* I = R + (size_t)(P - 2) * hs;
+    const int L = (n_chunks + P - 1) / P * kC;  // tokens per segment; the last one takes the rest
+    identity_kernel<<<kD, kD, 0, stream>>>(I);
+    bool ok = cudaGetLastError() == cudaSuccess;
+    runs.run[0] = {p.zero_init ? nullptr : p.state, Sst, one, 0, L};
+    for (int j = 1; j <= P - 2; ++j) {
+        runs.run[2 * j - 1] = {nullptr, X + (size_t)(j - 1) * hs, one, j * L, L};
+        runs.run[2 * j] = {I, R + (size_t)(j - 1) * hs, 0, j * L, L};  // every head from S0 = I
+    }
+    ok = ok && launch(runs, 2 * P - 3);
+    if (ok) {
+        prefill_combine_kernel<<<dim3(heads, kD / kCombCols), 256, kCombSmem, stream>>>(X, R, Sst, heads, P - 2);
+        ok = cudaGetLastError() == cudaSuccess;
+    }
+    if (ok) {
+        for (int j = 1; j <= P - 1; ++j) {
+            float* Sj = Sst + (size_t)(j - 1) * hs;
+            runs.run[j - 1] = {Sj, j == P - 1 ? p.state : Sj, one, j * L, j == P - 1 ? p.S - j * L : L};
+        }
+        ok = launch(runs, P - 1);
+    }
+    ok = cudaFreeAsync(ws, stream) == cudaSuccess && ok;
+    return ok ? GDN_OK : GDN_ERR_CUDA;
 }
 
 }  // namespace gdn

@@ -61,7 +61,10 @@ enum {
     GDN_ZERO_INITIAL_STATE = 1u << 0,
     /* Run the prefill on the fp32 FFMA kernel even where the tensor-core kernel
      * applies (a cross-check path; same results within fp32 rounding). */
-    GDN_FORCE_FFMA = 1u << 1
+    GDN_FORCE_FFMA = 1u << 1,
+    /* Never split a sequence into segments (see gdn_prefill): one pass over
+     * every sequence, whatever the SM count, so results do not depend on it. */
+    GDN_SINGLE_PASS = 1u << 2
 };
 
 /*
@@ -78,7 +81,7 @@ enum {
 typedef struct {
     int64_t B, Hk, Hv, S, Dk, Dv;
     int32_t dtype;   /* gdn_dtype */
-    uint32_t flags;  /* GDN_ZERO_INITIAL_STATE | GDN_FORCE_FFMA */
+    uint32_t flags;  /* GDN_ZERO_INITIAL_STATE | GDN_FORCE_FFMA | GDN_SINGLE_PASS */
 } gdn_dims;
 
 /*
@@ -100,6 +103,20 @@ typedef struct {
  * work is enqueued.  Implementation: Dk = Dv = 128 with bf16 runs on the
  * tcgen05 tensor-core kernel; every other supported shape and fp32 compute run
  * on the FFMA kernel.
+ *
+ * Few long sequences (on the tensor-core path, at most a third as many
+ * sequences B * Hv as SMs, and at least 24 chunks of 64 tokens each) are split
+ * into P >= 3 segments unless GDN_SINGLE_PASS is set.  The recurrence is affine
+ * in its start state, so a middle segment's end state is X + M S0, with X its
+ * end state from a zero start and M = (its end state from S0 = I) - X.  Three
+ * launches: segment 0 from the real start state together with both runs of
+ * every middle segment; a combine step that chains the maps into every
+ * segment's start state (fp32); segments 1 .. P - 1 from those start states,
+ * which write the outputs (a middle segment's outputs from the first launch
+ * are overwritten).  The scratch (3P - 5 states per sequence) is allocated with
+ * cudaMallocAsync on `stream` and freed there; if that allocation fails, the
+ * call runs one pass instead.  The results agree with the one-pass form within
+ * the bf16 tolerance, not bit for bit.
  */
 gdn_status gdn_prefill(const void* q, const void* k, const void* v,
                        const float* g_log, const float* beta, float scale,
@@ -276,8 +293,9 @@ gdn_status gdn_prefill_gated(const void* q, const void* k, const void* v, const 
                              const void* z, const float* norm_weight, float scale, float* state_inout, void* out,
                              const gdn_dims* dims, gdn_stream_t stream);
 
-/* Device workspace gdn_prefill needs for these dims: always 0 (every kernel
- * keeps its intermediates on chip). */
+/* Device workspace the caller must supply to gdn_prefill for these dims:
+ * always 0 (the single pass keeps its intermediates on chip; a split prefill
+ * allocates its own stream-ordered scratch). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);
 
 /* Static, NUL-terminated description of a status code. */

@@ -92,6 +92,15 @@ def test_empty_batch_is_a_no_op(L):
     assert _call(L, "gdn_decode_step", d) == gdn.GDN_OK
 
 
+def test_prefill_flags_known(L):
+    # every documented flag passes validation (B = 0: no CUDA call); the next bit does not
+    for f in (gdn.GDN_ZERO_INITIAL_STATE, gdn.GDN_FORCE_FFMA, gdn.GDN_SINGLE_PASS,
+              gdn.GDN_ZERO_INITIAL_STATE | gdn.GDN_SINGLE_PASS):
+        assert _call(L, "gdn_prefill", gdn.make_dims(0, 2, 4, 64, 128, 128, gdn.GDN_BF16, f)) == gdn.GDN_OK
+    assert _call(L, "gdn_prefill", gdn.make_dims(0, 2, 4, 64, 128, 128, gdn.GDN_BF16, 1 << 3)) == \
+        gdn.GDN_ERR_UNSUPPORTED
+
+
 def test_binding_requires_cuda_tensors():
     torch = pytest.importorskip("torch")
     q = torch.zeros(1, 1, 4, 8)
