@@ -529,6 +529,41 @@ def run_ours(args, rank, world, local_rank):
     block["sustained"]["method"] = "back-to-back calls over 3 input sets, each with its own weights and states"
     del xb, bws, bout, flush, bsets
 
+    # ---------------- long sequences (B=1, Hv=32, S=32768, zero start): the default form, which splits
+    #                  each sequence into segments over more SMs, against one pass (GDN_SINGLE_PASS)
+    wl = rank_workload(workloads.LONG_PREFILL, rank)
+    xl = workloads.make_inputs(wl, device=dev)
+    lout = torch.empty((wl.B, wl.Hv, wl.S, wl.Dv), dtype=wl.torch_dtype, device=dev)
+    lbytes, lflops = prefill_bytes(wl), prefill_flops(wl)
+
+    def long_leg(single_pass):
+        def step():
+            gdn.prefill(xl["q"], xl["k"], xl["v"], xl["g_log"], xl["beta"], xl["scale"], None, lout,
+                        single_pass=single_pass, stream=stream)
+        for _ in range(3):
+            step()
+        torch.cuda.synchronize()
+        evl = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(max(3, min(args.steps, 20)))]
+        for a, b in evl:
+            a.record(stream)
+            step()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = statistics.median([a.elapsed_time(b) for a, b in evl])
+        return {"ms": ms, "tokens_per_s": wl.B * wl.S / (ms * 1e-3) * world,
+                "hbm_frac": lbytes / (ms * 1e-3) / 1e9 / peaks["hbm"],
+                "tensor_frac": lflops / (ms * 1e-3) / 1e12 / peaks["bf16_sustained"]}
+
+    long_prefill = {"workload": wl.name, "split": long_leg(False), "single_pass": long_leg(True),
+                    "algorithmic_bytes": lbytes, "algorithmic_flops": lflops,
+                    "note": "split: segment 0 and two runs per middle segment, a combine step, then the "
+                            "remaining segments (2 prefill launches, an identity fill and the combine); "
+                            "inputs larger than L2"}
+    del xl, lout
+    if gdn.device_status(local_rank) != 0:
+        raise RuntimeError("a kernel reported a wait timeout")
+
     # ---------------- end to end through the public API from pinned host buffers
     # Every step copies its inputs and initial state from pinned host memory, runs gdn_prefill
     # and copies out and the final state back.  The copies of one step overlap the kernel and the
@@ -596,7 +631,7 @@ def run_ours(args, rank, world, local_rank):
         "config": {"workload": w.name, "B": w.B, "Hk": w.Hk, "Hv": w.Hv, "S": w.S, "Dk": w.Dk, "Dv": w.Dv,
                    "parallelism": "independent sequences per rank" if world > 1 else "single gpu",
                    "l2": "inputs larger than L2 (%.0f MB per step)" % (pbytes / 1e6)},
-        "roofline": roof, "prefill_gated": prefill_gated, "decode": decode, "decode_gated": gated, "decode_block": block, "conv1d": conv, "e2e": e2e, "clocks": clocks,
+        "roofline": roof, "prefill_gated": prefill_gated, "decode": decode, "decode_gated": gated, "decode_block": block, "conv1d": conv, "long_prefill": long_prefill, "e2e": e2e, "clocks": clocks,
         "gpu_launches": args.steps * gdn.kernels_per_call(),
         "launch_ms": {"median": statistics.median(launch_ms), "min": min(launch_ms), "max": max(launch_ms)},
     }

@@ -108,12 +108,13 @@ typedef struct {
  * sequences B * Hv as SMs, and at least 24 chunks of 64 tokens each) are split
  * into P >= 3 segments unless GDN_SINGLE_PASS is set.  The recurrence is affine
  * in its start state, so a middle segment's end state is X + M S0, with X its
- * end state from a zero start and M = (its end state from S0 = I) - X.  Three
- * launches: segment 0 from the real start state together with both runs of
- * every middle segment; a combine step that chains the maps into every
- * segment's start state (fp32); segments 1 .. P - 1 from those start states,
- * which write the outputs (a middle segment's outputs from the first launch
- * are overwritten).  The scratch (3P - 5 states per sequence) is allocated with
+ * end state from a zero start and M = (its end state from S0 = I) - X.  Four
+ * launches: an identity matrix; segment 0 from the real start state together
+ * with both runs of every middle segment; a combine step that chains the maps
+ * into every segment's start state (fp32); segments 1 .. P - 1 from those start
+ * states, which write the outputs (a middle segment's outputs from the second
+ * launch are overwritten).  The scratch (3P - 5 states per sequence and one
+ * identity) is allocated with
  * cudaMallocAsync on `stream` and freed there; if that allocation fails, the
  * call runs one pass instead.  The results agree with the one-pass form within
  * the bf16 tolerance, not bit for bit.
