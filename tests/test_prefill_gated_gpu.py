@@ -55,7 +55,9 @@ def test_rmsnorm_gated(gdn, dtype, rows, D, in_place):
 
 CASES = [workloads.TINY_PREFILL,
          workloads.PREFILL.with_(B=1, Hk=1, Hv=2, S=200, seed=31),
-         workloads.PREFILL.with_(B=2, Hk=2, Hv=4, S=130, state_std=0.0, seed=32)]
+         workloads.PREFILL.with_(B=2, Hk=2, Hv=4, S=130, state_std=0.0, seed=32),
+         # two long sequences: the prefill runs split into segments
+         workloads.PREFILL.with_(B=1, Hk=1, Hv=2, S=1800, seed=33)]
 
 
 @pytest.mark.parametrize("w", CASES, ids=lambda w: "%s_b%d_hv%d_s%d" % (w.dtype, w.B, w.Hv, w.S))
