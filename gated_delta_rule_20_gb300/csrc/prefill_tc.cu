@@ -295,7 +295,7 @@ struct PrefillRun {
     long long in_stride;    // Dk * Dv, or 0 (one start state for every head)
     int t0, len;            // len >= 1; every run but a sequence's last covers whole chunks
 };
-constexpr int kMaxRuns = 16;
+constexpr int kMaxRuns = 32;
 struct PrefillRuns {
     PrefillRun run[kMaxRuns];
     int heads;
@@ -914,11 +914,11 @@ bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_
 
 // ---------------------------------------------------------------- split sequences
 // Start states of the later segments of a split prefill (blockIdx.x = head, blockIdx.y = a
-// slice of kCombCols state columns): for j = 1 .. n_maps, S_{j+1} = (R_j - X_j) S_j + X_j.
+// slice of kCombCols state columns; 256 threads, thread t: row t / 2, 8 columns): for j = 1 .. n_maps, S_{j+1} = (R_j - X_j) S_j + X_j.
 // X_j is segment j's final state from a zero start and R_j the one from S0 = I; the chunk
 // recurrence is affine in its start state (S_end = M S0 + X), so R_j - X_j = M_j.  Each
 // state column evolves on its own, so the slices exchange nothing.  Plain fp32 FMAs.
-constexpr int kCombCols = 32;
+constexpr int kCombCols = 16;
 constexpr int kCombStride = kD + 1;  // padded rows of M: lane r of a warp reads bank (r + k) % 32
 constexpr size_t kCombSmem = (size_t)(kD * kCombStride + kD * kCombCols) * sizeof(float);
 
@@ -926,12 +926,13 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
                                                               float* __restrict__ Sst, int heads, int n_maps) {
     extern __shared__ float csm[];
     float* sM = csm;                     // [128][129]: R_j - X_j
-    float* sS = csm + kD * kCombStride;  // [128][32]: this slice of S_j
+    float* sS = csm + kD * kCombStride;  // [128][kCombCols]: this slice of S_j
     const int h = blockIdx.x, col0 = blockIdx.y * kCombCols, t = threadIdx.x;
     const size_t hs = (size_t)kD * kD;
     const float* S1 = Sst + (size_t)h * hs;
     for (int i = t; i < kD * kCombCols; i += 256) sS[i] = S1[(size_t)(i / kCombCols) * kD + col0 + i % kCombCols];
-    const int r = t >> 1, c0 = (t & 1) * 16;  // this thread: row r, columns c0 .. c0 + 15 of the slice
+    constexpr int kPer = kCombCols / 2;
+    const int r = t >> 1, c0 = (t & 1) * kPer;  // this thread: row r, columns c0 .. c0 + kPer - 1 of the slice
     for (int j = 1; j <= n_maps; ++j) {
         const float* Xj = X + ((size_t)(j - 1) * heads + h) * hs;
         const float* Rj = R + ((size_t)(j - 1) * heads + h) * hs;
@@ -945,15 +946,15 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
             d[3] = a.w - x.w;
         }
         __syncthreads();  // M_j and the S_j slice are complete
-        float acc[16];
+        float acc[kPer];
 #pragma unroll
-        for (int e = 0; e < 16; ++e) acc[e] = 0.f;
+        for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
 #pragma unroll 4
         for (int k = 0; k < kD; ++k) {
             const float m = sM[r * kCombStride + k];
             const float4* srow = reinterpret_cast<const float4*>(sS + k * kCombCols + c0);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
+            for (int q = 0; q < kPer / 4; ++q) {
                 const float4 v = srow[q];
                 acc[4 * q + 0] = fmaf(m, v.x, acc[4 * q + 0]);
                 acc[4 * q + 1] = fmaf(m, v.y, acc[4 * q + 1]);
@@ -964,7 +965,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
         __syncthreads();  // every thread has read M_j and S_j
         float* Sn = Sst + ((size_t)j * heads + h) * hs;  // S_{j+1}
 #pragma unroll
-        for (int e = 0; e < 16; ++e) {
+        for (int e = 0; e < kPer; ++e) {
             const size_t g = (size_t)r * kD + col0 + c0 + e;
             const float v = acc[e] + Xj[g];
             sS[r * kCombCols + c0 + e] = v;  // read in step j + 1 after its first barrier

@@ -25,7 +25,7 @@ def _status_clean():
     assert gdn.device_status(0, clear=True) == 0, "a kernel reported a wait timeout"
 
 
-def segments(heads, S, sms, max_runs=16):
+def segments(heads, S, sms, max_runs=32):
     """The segment count gdn_prefill picks (1: one pass); restated from its documented rule."""
     n = (S + 63) // 64
     if heads * 3 > sms:
