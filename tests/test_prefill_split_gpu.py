@@ -45,6 +45,9 @@ CASES = [
     ("b2_hk2_hv8_s3072_gqa4", 2, 2, 8, 3072, 0.05, (-0.5, -0.005), 1.0, 103, 5),
     ("b1_hv2_s3000_weak_decay", 1, 1, 2, 3000, 0.05, (-0.01, -0.0001), 1.0, 104, None),
     ("b1_hk2_hv4_s2500_strong_decay", 1, 2, 4, 2500, 0.05, (-2.0, -0.001), 2.0, 105, None),
+    # at the thresholds: 50 sequences (a third of 152 SMs: 150 CTAs in the first launch) and
+    # 24 chunks exactly (3 segments of 8 chunks)
+    ("b2_hk5_hv25_s1536_threshold", 2, 5, 25, 1536, 0.02, (-0.5, -0.005), 1.0, 106, 4),
 ]
 
 
@@ -74,7 +77,8 @@ def _picks(w, n, seed):
 def test_split_prefill_matches_oracle(case):
     w, x = _inputs(case)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
-    assert segments(w.B * w.Hv, w.S, sms) >= 3, "the case must take the split path"
+    if segments(w.B * w.Hv, w.S, sms) < 3:  # every case splits on a 152-SM GB300
+        pytest.skip("not split on a GPU with %d SMs" % sms)
     out, st = _run(x)
     picks = _picks(w, case[-1], case[8])
     ro, rs = oracle_for(x, picks, w.Hv // w.Hk)
