@@ -913,63 +913,84 @@ bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_
 }
 
 // ---------------------------------------------------------------- split sequences
-// Start states of the later segments of a split prefill (blockIdx.x = head, blockIdx.y = a
-// slice of kCombCols state columns; 256 threads, thread t: row t / 2, 8 columns): for j = 1 .. n_maps, S_{j+1} = (R_j - X_j) S_j + X_j.
-// X_j is segment j's final state from a zero start and R_j the one from S0 = I; the chunk
-// recurrence is affine in its start state (S_end = M S0 + X), so R_j - X_j = M_j.  Each
-// state column evolves on its own, so the slices exchange nothing.  Plain fp32 FMAs.
-constexpr int kCombCols = 16;
-constexpr int kCombStride = kD + 1;  // padded rows of M: lane r of a warp reads bank (r + k) % 32
-constexpr size_t kCombSmem = (size_t)(kD * kCombStride + kD * kCombCols) * sizeof(float);
+// Start states of the later segments of a split prefill: for j = 1 .. n_maps,
+//     S_{j+1} = (R_j - X_j) S_j + X_j,
+// X_j being segment j's final state from a zero start and R_j the one from S0 = I; the
+// chunk recurrence is affine in its start state (S_end = M S0 + X), so R_j - X_j = M_j.
+// Each state column evolves on its own: blockIdx.x = head, blockIdx.y = a slice of kCols
+// columns, and the slices exchange nothing.  256 threads, thread t: row t / 2, kCols / 2
+// columns; plain fp32 FMAs.  R_{j+1} and X_{j+1} reach shared memory by cp.async while
+// step j computes, so each step pays one copy latency at most.
+constexpr int kCombStride = kD + 4;  // padded rows of M, 16-byte aligned: the 16 rows a warp reads
+                                     // fall on 8 distinct 16-byte bank groups
+template <int kCols>
+constexpr size_t comb_smem() {  // raw R_j, X_j; M_j; the S_j and X_j slices
+    return (size_t)(2 * kD * kD + kD * kCombStride + 2 * kD * kCols) * sizeof(float);
+}
 
+template <int kCols>
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ X, const float* __restrict__ R,
                                                               float* __restrict__ Sst, int heads, int n_maps) {
-    extern __shared__ float csm[];
-    float* sM = csm;                     // [128][129]: R_j - X_j
-    float* sS = csm + kD * kCombStride;  // [128][kCombCols]: this slice of S_j
-    const int h = blockIdx.x, col0 = blockIdx.y * kCombCols, t = threadIdx.x;
+    extern __shared__ __align__(16) float csm[];
+    float* rawR = csm;                  // [128][128] R_j as copied
+    float* rawX = rawR + kD * kD;       // [128][128] X_j
+    float* sM = rawX + kD * kD;         // [128][129] M_j
+    float* sS = sM + kD * kCombStride;  // [128][kCols] this slice of S_j
+    float* sX = sS + kD * kCols;        // [128][kCols] this slice of X_j
+    const int h = blockIdx.x, col0 = blockIdx.y * kCols, t = threadIdx.x;
     const size_t hs = (size_t)kD * kD;
-    const float* S1 = Sst + (size_t)h * hs;
-    for (int i = t; i < kD * kCombCols; i += 256) sS[i] = S1[(size_t)(i / kCombCols) * kD + col0 + i % kCombCols];
-    constexpr int kPer = kCombCols / 2;
-    const int r = t >> 1, c0 = (t & 1) * kPer;  // this thread: row r, columns c0 .. c0 + kPer - 1 of the slice
-    for (int j = 1; j <= n_maps; ++j) {
-        const float* Xj = X + ((size_t)(j - 1) * heads + h) * hs;
+    auto copy_maps = [&](int j) {
         const float* Rj = R + ((size_t)(j - 1) * heads + h) * hs;
+        const float* Xj = X + ((size_t)(j - 1) * heads + h) * hs;
         for (int i = t; i < kD * kD / 4; i += 256) {
-            const float4 a = reinterpret_cast<const float4*>(Rj)[i];
-            const float4 x = reinterpret_cast<const float4*>(Xj)[i];
-            float* d = sM + (4 * i / kD) * kCombStride + 4 * i % kD;
-            d[0] = a.x - x.x;
-            d[1] = a.y - x.y;
-            d[2] = a.z - x.z;
-            d[3] = a.w - x.w;
+            cp_async_16(rawR + 4 * i, Rj + 4 * i);
+            cp_async_16(rawX + 4 * i, Xj + 4 * i);
         }
-        __syncthreads();  // M_j and the S_j slice are complete
+        cp_async_commit();
+    };
+    copy_maps(1);
+    const float* S1 = Sst + (size_t)h * hs;
+    for (int i = t; i < kD * kCols; i += 256) sS[i] = S1[(size_t)(i / kCols) * kD + col0 + i % kCols];
+    constexpr int kPer = kCols / 2;
+    const int r = t >> 1, c0 = (t & 1) * kPer;
+    for (int j = 1; j <= n_maps; ++j) {
+        cp_async_wait_all();
+        __syncthreads();  // R_j, X_j and the S_j slice are in shared memory
+        for (int i = t; i < kD * kD / 4; i += 256) {
+            const float4 a = reinterpret_cast<const float4*>(rawR)[i];
+            const float4 x = reinterpret_cast<const float4*>(rawX)[i];
+            *reinterpret_cast<float4*>(sM + (4 * i / kD) * kCombStride + 4 * i % kD) =
+                make_float4(a.x - x.x, a.y - x.y, a.z - x.z, a.w - x.w);
+        }
+        for (int i = t; i < kD * kCols; i += 256) sX[i] = rawX[(i / kCols) * kD + col0 + i % kCols];
+        __syncthreads();  // M_j and the X_j slice are built; the raw buffers are free
+        if (j < n_maps) copy_maps(j + 1);
         float acc[kPer];
 #pragma unroll
         for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-#pragma unroll 4
-        for (int k = 0; k < kD; ++k) {
-            const float m = sM[r * kCombStride + k];
-            const float4* srow = reinterpret_cast<const float4*>(sS + k * kCombCols + c0);
+        for (int k = 0; k < kD; k += 4) {  // four k per 16-byte read of M's row
+            const float4 m4 = *reinterpret_cast<const float4*>(sM + r * kCombStride + k);
+            const float mk[4] = {m4.x, m4.y, m4.z, m4.w};
 #pragma unroll
-            for (int q = 0; q < kPer / 4; ++q) {
-                const float4 v = srow[q];
-                acc[4 * q + 0] = fmaf(m, v.x, acc[4 * q + 0]);
-                acc[4 * q + 1] = fmaf(m, v.y, acc[4 * q + 1]);
-                acc[4 * q + 2] = fmaf(m, v.z, acc[4 * q + 2]);
-                acc[4 * q + 3] = fmaf(m, v.w, acc[4 * q + 3]);
+            for (int kk = 0; kk < 4; ++kk) {
+                const float4* srow = reinterpret_cast<const float4*>(sS + (k + kk) * kCols + c0);
+#pragma unroll
+                for (int q = 0; q < kPer / 4; ++q) {
+                    const float4 v = srow[q];
+                    acc[4 * q + 0] = fmaf(mk[kk], v.x, acc[4 * q + 0]);
+                    acc[4 * q + 1] = fmaf(mk[kk], v.y, acc[4 * q + 1]);
+                    acc[4 * q + 2] = fmaf(mk[kk], v.z, acc[4 * q + 2]);
+                    acc[4 * q + 3] = fmaf(mk[kk], v.w, acc[4 * q + 3]);
+                }
             }
         }
-        __syncthreads();  // every thread has read M_j and S_j
+        __syncthreads();  // every thread has read the S_j slice
         float* Sn = Sst + ((size_t)j * heads + h) * hs;  // S_{j+1}
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {
-            const size_t g = (size_t)r * kD + col0 + c0 + e;
-            const float v = acc[e] + Xj[g];
-            sS[r * kCombCols + c0 + e] = v;  // read in step j + 1 after its first barrier
-            Sn[g] = v;
+            const float v = acc[e] + sX[r * kCols + c0 + e];
+            sS[r * kCols + c0 + e] = v;  // read in step j + 1 after its first barrier
+            Sn[(size_t)r * kD + col0 + c0 + e] = v;
         }
     }
 }
@@ -1017,8 +1038,10 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
                                      (int)SMEM_ALLOC) != cudaSuccess ||
                 cudaFuncSetAttribute(gdn_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SMEM_ALLOC) != cudaSuccess ||
-                cudaFuncSetAttribute(prefill_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)kCombSmem) != cudaSuccess ||
+                cudaFuncSetAttribute(prefill_combine_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)comb_smem<16>()) != cudaSuccess ||
+                cudaFuncSetAttribute(prefill_combine_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)comb_smem<32>()) != cudaSuccess ||
                 cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return GDN_ERR_CUDA;
             configured[dev] = true;
@@ -1064,7 +1087,11 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     }
     ok = ok && launch(runs, 2 * P - 3);
     if (ok) {
-        prefill_combine_kernel<<<dim3(heads, kD / kCombCols), 256, kCombSmem, stream>>>(X, R, Sst, heads, P - 2);
+        // one CTA per SM (about 210 KB of shared memory): 16-column slices while they fit one wave
+        if (heads * (kD / 16) <= sm_count[dev])
+            prefill_combine_kernel<16><<<dim3(heads, kD / 16), 256, comb_smem<16>(), stream>>>(X, R, Sst, heads, P - 2);
+        else
+            prefill_combine_kernel<32><<<dim3(heads, kD / 32), 256, comb_smem<32>(), stream>>>(X, R, Sst, heads, P - 2);
         ok = cudaGetLastError() == cudaSuccess;
     }
     if (ok) {
