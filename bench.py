@@ -557,9 +557,9 @@ def run_ours(args, rank, world, local_rank):
 
     long_prefill = {"workload": wl.name, "split": long_leg(False), "single_pass": long_leg(True),
                     "algorithmic_bytes": lbytes, "algorithmic_flops": lflops,
-                    "note": "split: segment 0 and two runs per middle segment, a combine step, then the "
-                            "remaining segments (2 prefill launches, an identity fill and the combine); "
-                            "inputs larger than L2"}
+                    "note": "split: segment 0 and two state-only runs per middle segment, a combine step, "
+                            "then the remaining segments (2 prefill launches, an identity fill and the "
+                            "combine); inputs larger than L2"}
     del xl, lout
     if gdn.device_status(local_rank) != 0:
         raise RuntimeError("a kernel reported a wait timeout")

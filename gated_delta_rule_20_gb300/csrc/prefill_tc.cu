@@ -294,6 +294,7 @@ struct PrefillRun {
     float* state_out;       // final states [heads, Dk, Dv]; may equal state_in
     long long in_stride;    // Dk * Dv, or 0 (one start state for every head)
     int t0, len;            // len >= 1; every run but a sequence's last covers whole chunks
+    int write_out;          // 0: the outputs are not stored (a run that only yields a state)
 };
 constexpr int kMaxRuns = 32;
 struct PrefillRuns {
@@ -837,7 +838,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars->dfree[dbp]);  // the U/W product may reuse R_D[dbp]
                 fence_proxy_async_smem();
                 named_bar_sync(BAR_HELP, kHelp);
-                if (ht == 0) {
+                if (ht == 0 && (!kSplit || runs.run[ri].write_out)) {
                     tma_store_3d(&tm_o, sm + OFF_OUT, 0, tb + p * kC, bh);
                     tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, tb + p * kC, bh);
                     tma_store_commit();
@@ -1070,7 +1071,7 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
         ws = nullptr;
     }
     if (!ws) {  // one run over the whole sequence
-        runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S};
+        runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S, 1};
         return launch(runs, 1) ? GDN_OK : GDN_ERR_CUDA;
     }
     float* Sst = static_cast<float*>(ws);
@@ -1080,10 +1081,10 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     const int L = (n_chunks + P - 1) / P * kC;  // tokens per segment; the last one takes the rest
     identity_kernel<<<kD, kD, 0, stream>>>(I);
     bool ok = cudaGetLastError() == cudaSuccess;
-    runs.run[0] = {p.zero_init ? nullptr : p.state, Sst, one, 0, L};
-    for (int j = 1; j <= P - 2; ++j) {
-        runs.run[2 * j - 1] = {nullptr, X + (size_t)(j - 1) * hs, one, j * L, L};
-        runs.run[2 * j] = {I, R + (size_t)(j - 1) * hs, 0, j * L, L};  // every head from S0 = I
+    runs.run[0] = {p.zero_init ? nullptr : p.state, Sst, one, 0, L, 1};
+    for (int j = 1; j <= P - 2; ++j) {  // the map runs store no outputs
+        runs.run[2 * j - 1] = {nullptr, X + (size_t)(j - 1) * hs, one, j * L, L, 0};
+        runs.run[2 * j] = {I, R + (size_t)(j - 1) * hs, 0, j * L, L, 0};  // every head from S0 = I
     }
     ok = ok && launch(runs, 2 * P - 3);
     if (ok) {
@@ -1097,7 +1098,7 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     if (ok) {
         for (int j = 1; j <= P - 1; ++j) {
             float* Sj = Sst + (size_t)(j - 1) * hs;
-            runs.run[j - 1] = {Sj, j == P - 1 ? p.state : Sj, one, j * L, j == P - 1 ? p.S - j * L : L};
+            runs.run[j - 1] = {Sj, j == P - 1 ? p.state : Sj, one, j * L, j == P - 1 ? p.S - j * L : L, 1};
         }
         ok = launch(runs, P - 1);
     }

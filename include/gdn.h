@@ -112,9 +112,10 @@ typedef struct {
  * launches: an identity matrix; segment 0 from the real start state together
  * with both runs of every middle segment; a combine step that chains the maps
  * into every segment's start state (fp32); segments 1 .. P - 1 from those start
- * states, which write the outputs (a middle segment's outputs from the second
- * launch are overwritten).  The scratch (3P - 5 states per sequence and one
- * identity) is allocated with
+ * states.  Every output element is written once, by the run that owns its
+ * token (the zero- and identity-start runs store none), so out is written as
+ * in one pass.  The scratch (3P - 5 states per sequence and one identity) is
+ * allocated with
  * cudaMallocAsync on `stream` and freed there; if that allocation fails, the
  * call runs one pass instead.  The results agree with the one-pass form within
  * the bf16 tolerance, not bit for bit.

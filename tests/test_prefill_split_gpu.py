@@ -4,7 +4,7 @@ states come from each middle segment's end states from a zero and an identity st
 chunk recurrence is affine in its start state).  Checked here: parity with the fp64 oracle,
 agreement with the one-pass form (GDN_SINGLE_PASS), a ragged last segment, zero and supplied
 start states, GQA, weak decay (so that every segment's state map matters), strong decay,
-determinism and replay in a CUDA graph."""
+determinism, NaN-prefilled outputs with guard bands, and replay in a CUDA graph."""
 import numpy as np
 import pytest
 import torch
@@ -112,6 +112,16 @@ def test_split_prefill_is_taken():
     o1, _ = _run(x)
     o2, _ = _run(x, single_pass=True)
     assert not torch.equal(o1, o2)
+
+
+def test_split_prefill_writes_every_output_once():
+    """Outputs pre-filled with NaN and guard elements around out and state: the split form
+    writes every output element (no NaN left) and nothing outside the buffers."""
+    from gpu_util import run_prefill
+    _, x = _inputs(CASES[0])
+    out, st = run_prefill(x, guard=256)
+    o2, s2 = _run(x)
+    assert torch.equal(out, o2) and torch.equal(st, s2)
 
 
 def test_split_prefill_deterministic():
