@@ -264,24 +264,25 @@ __device__ __forceinline__ void solve_diag_block(float* M, int blk, int lane) {
 }
 
 // ---------------------------------------------------------------- TMA
+// q, k of tokens t0 .. t0 + 63 of key head bhk; v from the box at (vt, vh) of tv
 __device__ __forceinline__ void load_chunk(uint8_t* st, uint64_t* bar, const CUtensorMap* tq, const CUtensorMap* tk,
-                                           const CUtensorMap* tv, int t0, int bhk, int bh) {
+                                           const CUtensorMap* tv, int t0, int bhk, int vt, int vh) {
     mbar_arrive_expect_tx(bar, LOAD_BYTES);
     tma_load_3d(st + ST_K0, tk, bar, 0, t0, bhk);
     tma_load_3d(st + ST_Q0, tq, bar, 0, t0, bhk);
     tma_load_3d(st + ST_K1, tk, bar, 64, t0, bhk);
     tma_load_3d(st + ST_Q1, tq, bar, 64, t0, bhk);
-    tma_load_3d(st + ST_VW0, tv, bar, 0, t0, bh);
-    tma_load_3d(st + ST_VW1, tv, bar, 64, t0, bh);
+    tma_load_3d(st + ST_VW0, tv, bar, 0, vt, vh);
+    tma_load_3d(st + ST_VW1, tv, bar, 64, vt, vh);
 }
 __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                                                  int t0, int bhk, int bh) {
+                                                  int t0, int bhk, int vt, int vh) {
     tma_prefetch_l2_3d(tk, 0, t0, bhk);
     tma_prefetch_l2_3d(tk, 64, t0, bhk);
     tma_prefetch_l2_3d(tq, 0, t0, bhk);
     tma_prefetch_l2_3d(tq, 64, t0, bhk);
-    tma_prefetch_l2_3d(tv, 0, t0, bh);
-    tma_prefetch_l2_3d(tv, 64, t0, bh);
+    tma_prefetch_l2_3d(tv, 0, vt, vh);
+    tma_prefetch_l2_3d(tv, 64, vt, vh);
 }
 
 // ---------------------------------------------------------------- kernel
@@ -295,6 +296,7 @@ struct PrefillRun {
     long long in_stride;    // Dk * Dv, or 0 (one start state for every head)
     int t0, len;            // len >= 1; every run but a sequence's last covers whole chunks
     int write_out;          // 0: the outputs are not stored (a run that only yields a state)
+    int zero_v;             // 1: v = 0 (every chunk's v tile read from the 64-token zero map)
 };
 constexpr int kMaxRuns = 32;
 struct PrefillRuns {
@@ -308,6 +310,7 @@ template <bool kSplit>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                          const __grid_constant__ CUtensorMap tm_v0,
                           const float* __restrict__ g_log, const float* __restrict__ beta,
                           const __grid_constant__ PrefillRuns runs, float scale, int Hk, int Hv, int S,
                           int32_t* __restrict__ status) {
@@ -785,16 +788,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // store, and the input loads.  Thread ht reads TMEM lanes 32 (warp % 4) + ...
         const int ht = tid - kPrep - kChain;
         int last_load = -1;  // chunks are loaded in order; this is the last one (thread ht == 0 loads)
+        // v of the run (a map run of a split reads the zero tile for every chunk)
+        const bool zero_v = kSplit && runs.run[ri].zero_v;
+        const CUtensorMap* tv_run = zero_v ? &tm_v0 : &tm_v;
+        const int vh = zero_v ? 0 : bh;
+        auto vt_of = [&](int t) { return zero_v ? 0 : t; };
         if (ht == 0) {
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
-            tma_prefetch_desc(&tm_v);
+            tma_prefetch_desc(tv_run);
             tma_prefetch_desc(&tm_o);
             for (int c = 0; c < kStages && c < n_chunks; ++c) {
-                load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, &tm_v, tb + c * kC, bhk, bh);
+                const int t = tb + c * kC;
+                load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, tv_run, t, bhk, vt_of(t), vh);
                 last_load = c;
             }
-            if (n_chunks > kStages) prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, tb + kStages * kC, bhk, bh);
+            if (n_chunks > kStages) {
+                const int t = tb + kStages * kC;
+                prefetch_chunk_l2(&tm_q, &tm_k, tv_run, t, bhk, vt_of(t), vh);
+            }
         }
         int issued3 = -1;  // last chunk whose output product was committed
         // Iteration c: the output of chunk c - 1 (its product, the tile, the store, the stage
@@ -824,11 +836,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (named_bar_any(BAR_HELP, kHelp, fail)) break;
                 if (ht == 0 && p + kStages < n_chunks) {
                     // reload the stage with chunk p + kStages and prefetch the chunk after into L2
-                    load_chunk(sm + sp * STAGE_BYTES, &bars->full[sp], &tm_q, &tm_k, &tm_v, tb + (p + kStages) * kC,
-                               bhk, bh);
+                    const int t = tb + (p + kStages) * kC;
+                    load_chunk(sm + sp * STAGE_BYTES, &bars->full[sp], &tm_q, &tm_k, tv_run, t, bhk, vt_of(t), vh);
                     last_load = p + kStages;
                     if (p + kStages + 1 < n_chunks)
-                        prefetch_chunk_l2(&tm_q, &tm_k, &tm_v, tb + (p + kStages + 1) * kC, bhk, bh);
+                        prefetch_chunk_l2(&tm_q, &tm_k, tv_run, t + kC, bhk, vt_of(t + kC), vh);
                 }
                 if (ht == 0) tma_store_wait_read0();  // the out tile of chunk p - 1 has been read
                 named_bar_sync(BAR_HELP, kHelp);
@@ -915,36 +927,36 @@ bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_
 
 // ---------------------------------------------------------------- split sequences
 // Start states of the later segments of a split prefill: for j = 1 .. n_maps,
-//     S_{j+1} = (R_j - X_j) S_j + X_j,
-// X_j being segment j's final state from a zero start and R_j the one from S0 = I; the
-// chunk recurrence is affine in its start state (S_end = M S0 + X), so R_j - X_j = M_j.
-// Each state column evolves on its own: blockIdx.x = head, blockIdx.y = a slice of kCols
-// columns, and the slices exchange nothing.  256 threads, thread t: row t / 2, kCols / 2
-// columns; plain fp32 FMAs.  R_{j+1} and X_{j+1} reach shared memory by cp.async while
-// step j computes, so each step pays one copy latency at most.
+//     S_{j+1} = M_j S_j + X_j.
+// The chunk recurrence is affine in its start state (S_end = M S0 + X): X_j is segment j's
+// final state from a zero start, M_j its final state from S0 = I with v = 0.  Each state
+// column evolves on its own: blockIdx.x = head, blockIdx.y = a slice of kCols columns, and
+// the slices exchange nothing.  256 threads, thread t: row t / 2, kCols / 2 columns; plain
+// fp32 FMAs.  M_{j+1} and X_{j+1} reach shared memory by cp.async while step j computes,
+// so each step pays one copy latency at most.
 constexpr int kCombStride = kD + 4;  // padded rows of M, 16-byte aligned: the 16 rows a warp reads
                                      // fall on 8 distinct 16-byte bank groups
 template <int kCols>
-constexpr size_t comb_smem() {  // raw R_j, X_j; M_j; the S_j and X_j slices
+constexpr size_t comb_smem() {  // raw M_j, X_j; M_j with padded rows; the S_j and X_j slices
     return (size_t)(2 * kD * kD + kD * kCombStride + 2 * kD * kCols) * sizeof(float);
 }
 
 template <int kCols>
-__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ X, const float* __restrict__ R,
+__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ X, const float* __restrict__ Mg,
                                                               float* __restrict__ Sst, int heads, int n_maps) {
     extern __shared__ __align__(16) float csm[];
-    float* rawR = csm;                  // [128][128] R_j as copied
-    float* rawX = rawR + kD * kD;       // [128][128] X_j
+    float* rawM = csm;                  // [128][128] M_j as copied
+    float* rawX = rawM + kD * kD;       // [128][128] X_j
     float* sM = rawX + kD * kD;         // [128][129] M_j
     float* sS = sM + kD * kCombStride;  // [128][kCols] this slice of S_j
     float* sX = sS + kD * kCols;        // [128][kCols] this slice of X_j
     const int h = blockIdx.x, col0 = blockIdx.y * kCols, t = threadIdx.x;
     const size_t hs = (size_t)kD * kD;
     auto copy_maps = [&](int j) {
-        const float* Rj = R + ((size_t)(j - 1) * heads + h) * hs;
+        const float* Mj = Mg + ((size_t)(j - 1) * heads + h) * hs;
         const float* Xj = X + ((size_t)(j - 1) * heads + h) * hs;
         for (int i = t; i < kD * kD / 4; i += 256) {
-            cp_async_16(rawR + 4 * i, Rj + 4 * i);
+            cp_async_16(rawM + 4 * i, Mj + 4 * i);
             cp_async_16(rawX + 4 * i, Xj + 4 * i);
         }
         cp_async_commit();
@@ -956,13 +968,10 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
     const int r = t >> 1, c0 = (t & 1) * kPer;
     for (int j = 1; j <= n_maps; ++j) {
         cp_async_wait_all();
-        __syncthreads();  // R_j, X_j and the S_j slice are in shared memory
-        for (int i = t; i < kD * kD / 4; i += 256) {
-            const float4 a = reinterpret_cast<const float4*>(rawR)[i];
-            const float4 x = reinterpret_cast<const float4*>(rawX)[i];
+        __syncthreads();  // M_j, X_j and the S_j slice are in shared memory
+        for (int i = t; i < kD * kD / 4; i += 256)
             *reinterpret_cast<float4*>(sM + (4 * i / kD) * kCombStride + 4 * i % kD) =
-                make_float4(a.x - x.x, a.y - x.y, a.z - x.z, a.w - x.w);
-        }
+                reinterpret_cast<const float4*>(rawM)[i];
         for (int i = t; i < kD * kCols; i += 256) sX[i] = rawX[(i / kCols) * kD + col0 + i % kCols];
         __syncthreads();  // M_j and the X_j slice are built; the raw buffers are free
         if (j < n_maps) copy_maps(j + 1);
@@ -1049,13 +1058,14 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
         }
     }
     const int heads = p.B * p.Hv;
+    CUtensorMap tv0 = tv;  // the zero v tile of a split's map runs (unused by one-pass launches)
     auto launch = [&](const PrefillRuns& runs, int n_runs) {
         if (n_runs == 1 && runs.run[0].t0 == 0 && runs.run[0].len == p.S)
             gdn_prefill_tc_kernel<false><<<heads, kThreads, SMEM_ALLOC, stream>>>(
-                tq, tk, tv, to, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+                tq, tk, tv, to, tv0, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
         else
             gdn_prefill_tc_kernel<true><<<heads * n_runs, kThreads, SMEM_ALLOC, stream>>>(
-                tq, tk, tv, to, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+                tq, tk, tv, to, tv0, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
         return cudaGetLastError() == cudaSuccess;
     };
     PrefillRuns runs{};
@@ -1065,40 +1075,46 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     const size_t hs = (size_t)heads * kD * kD;  // floats in one state per head
     const long long one = (long long)kD * kD;  // floats in one head's state
     void* ws = nullptr;
-    // stream-ordered scratch: S_1 .. S_{P-1}, X_1 .. X_{P-2}, R_1 .. R_{P-2}, and one identity
-    if (P > 1 && cudaMallocAsync(&ws, ((size_t)(3 * P - 5) * hs + one) * sizeof(float), stream) != cudaSuccess) {
+    // stream-ordered scratch: S_1 .. S_{P-1}, X_1 .. X_{P-2}, M_1 .. M_{P-2}, one identity and
+    // one zero v tile [64 tokens][128] bf16
+    constexpr size_t kZeroTile = (size_t)kC * kD * 2;
+    if (P > 1 &&
+        cudaMallocAsync(&ws, ((size_t)(3 * P - 5) * hs + one) * sizeof(float) + kZeroTile, stream) != cudaSuccess) {
         (void)cudaGetLastError();
         ws = nullptr;
     }
     if (!ws) {  // one run over the whole sequence
-        runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S, 1};
+        runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S, 1, 0};
         return launch(runs, 1) ? GDN_OK : GDN_ERR_CUDA;
     }
     float* Sst = static_cast<float*>(ws);
     float* X = Sst + (size_t)(P - 1) * hs;
-    float* R = X + (size_t)(P - 2) * hs;
-    float* I = R + (size_t)(P - 2) * hs;
+    float* M = X + (size_t)(P - 2) * hs;
+    float* I = M + (size_t)(P - 2) * hs;
+    void* Z = I + one;
     const int L = (n_chunks + P - 1) / P * kC;  // tokens per segment; the last one takes the rest
     identity_kernel<<<kD, kD, 0, stream>>>(I);
-    bool ok = cudaGetLastError() == cudaSuccess;
-    runs.run[0] = {p.zero_init ? nullptr : p.state, Sst, one, 0, L, 1};
+    bool ok = cudaGetLastError() == cudaSuccess && cudaMemsetAsync(Z, 0, kZeroTile, stream) == cudaSuccess &&
+              encode_bf16_3d(&tv0, Z, 1, kC, 64, true);
+    runs.run[0] = {p.zero_init ? nullptr : p.state, Sst, one, 0, L, 1, 0};
     for (int j = 1; j <= P - 2; ++j) {  // the map runs store no outputs
-        runs.run[2 * j - 1] = {nullptr, X + (size_t)(j - 1) * hs, one, j * L, L, 0};
-        runs.run[2 * j] = {I, R + (size_t)(j - 1) * hs, 0, j * L, L, 0};  // every head from S0 = I
+        runs.run[2 * j - 1] = {nullptr, X + (size_t)(j - 1) * hs, one, j * L, L, 0, 0};
+        // from S0 = I with v = 0: the end state is the segment's linear map M_j itself
+        runs.run[2 * j] = {I, M + (size_t)(j - 1) * hs, 0, j * L, L, 0, 1};
     }
     ok = ok && launch(runs, 2 * P - 3);
     if (ok) {
         // one CTA per SM (about 210 KB of shared memory): 16-column slices while they fit one wave
         if (heads * (kD / 16) <= sm_count[dev])
-            prefill_combine_kernel<16><<<dim3(heads, kD / 16), 256, comb_smem<16>(), stream>>>(X, R, Sst, heads, P - 2);
+            prefill_combine_kernel<16><<<dim3(heads, kD / 16), 256, comb_smem<16>(), stream>>>(X, M, Sst, heads, P - 2);
         else
-            prefill_combine_kernel<32><<<dim3(heads, kD / 32), 256, comb_smem<32>(), stream>>>(X, R, Sst, heads, P - 2);
+            prefill_combine_kernel<32><<<dim3(heads, kD / 32), 256, comb_smem<32>(), stream>>>(X, M, Sst, heads, P - 2);
         ok = cudaGetLastError() == cudaSuccess;
     }
     if (ok) {
         for (int j = 1; j <= P - 1; ++j) {
             float* Sj = Sst + (size_t)(j - 1) * hs;
-            runs.run[j - 1] = {Sj, j == P - 1 ? p.state : Sj, one, j * L, j == P - 1 ? p.S - j * L : L, 1};
+            runs.run[j - 1] = {Sj, j == P - 1 ? p.state : Sj, one, j * L, j == P - 1 ? p.S - j * L : L, 1, 0};
         }
         ok = launch(runs, P - 1);
     }

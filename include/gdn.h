@@ -108,7 +108,7 @@ typedef struct {
  * sequences B * Hv as SMs, and at least 24 chunks of 64 tokens each) are split
  * into P >= 3 segments unless GDN_SINGLE_PASS is set.  The recurrence is affine
  * in its start state, so a middle segment's end state is X + M S0, with X its
- * end state from a zero start and M = (its end state from S0 = I) - X.  Four
+ * end state from a zero start and M its end state from S0 = I with v = 0.  Four
  * launches: an identity matrix; segment 0 from the real start state together
  * with both runs of every middle segment; a combine step that chains the maps
  * into every segment's start state (fp32); segments 1 .. P - 1 from those start
@@ -117,8 +117,9 @@ typedef struct {
  * in one pass.  The scratch (3P - 5 states per sequence and one identity) is
  * allocated with
  * cudaMallocAsync on `stream` and freed there; if that allocation fails, the
- * call runs one pass instead.  The results agree with the one-pass form within
- * the bf16 tolerance, not bit for bit.
+ * call runs one pass instead.  The results agree with the one-pass form to
+ * within rounding (the same error against an fp64 reference, from strong decay
+ * to none), not bit for bit.
  */
 gdn_status gdn_prefill(const void* q, const void* k, const void* v,
                        const float* g_log, const float* beta, float scale,

@@ -45,6 +45,8 @@ CASES = [
     ("b2_hk2_hv8_s3072_gqa4", 2, 2, 8, 3072, 0.05, (-0.5, -0.005), 1.0, 103, 5),
     ("b1_hv2_s3000_weak_decay", 1, 1, 2, 3000, 0.05, (-0.01, -0.0001), 1.0, 104, None),
     ("b1_hk2_hv4_s2500_strong_decay", 1, 2, 4, 2500, 0.05, (-2.0, -0.001), 2.0, 105, None),
+    # almost no decay: the state persists through every segment, so the maps carry it
+    ("b1_hv2_s4096_almost_no_decay", 1, 1, 2, 4096, 0.05, (-1e-4, -1e-6), 1.0, 107, None),
     # at the thresholds: 50 sequences (a third of 152 SMs: 150 CTAs in the first launch) and
     # 24 chunks exactly (3 segments of 8 chunks)
     ("b2_hk5_hv25_s1536_threshold", 2, 5, 25, 1536, 0.02, (-0.5, -0.005), 1.0, 106, 4),
