@@ -33,7 +33,7 @@ GDN_SINGLE_PASS = 1 << 2
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
             "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
             "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block", "gdn_rmsnorm_gated",
-            "gdn_prefill_gated")
+            "gdn_prefill_gated", "gdn_prefill_segments")
 
 
 class GdnDims(ctypes.Structure):
@@ -84,6 +84,8 @@ def lib() -> ctypes.CDLL:
         L.gdn_device_status.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]
         L.gdn_kernels_per_call.restype = ctypes.c_int
         L.gdn_kernels_per_call.argtypes = []
+        L.gdn_prefill_segments.restype = ctypes.c_int32
+        L.gdn_prefill_segments.argtypes = [ctypes.POINTER(GdnDims), ctypes.c_int32]
         L.gdn_decode_gated.restype = ctypes.c_int
         L.gdn_decode_gated.argtypes = [vp, vp, vp, vp, fp, fp, fp, ctypes.c_float, fp, vp, ctypes.POINTER(GdnDims),
                                        vp]
@@ -259,6 +261,17 @@ def device_status(device: int = 0, clear: bool = True) -> int:
 
 def kernels_per_call() -> int:
     return int(lib().gdn_kernels_per_call())
+
+
+def prefill_segments(B, Hk, Hv, S, Dk=128, Dv=128, dtype=GDN_BF16, sm_count=None, *, single_pass=False,
+                     force_ffma=False) -> int:
+    """``gdn_prefill_segments``: the segments gdn_prefill splits each sequence into (1: one
+    pass) on a device with ``sm_count`` SMs (default: the current CUDA device's)."""
+    if sm_count is None:
+        sm_count = _torch().cuda.get_device_properties(_torch().cuda.current_device()).multi_processor_count
+    flags = (GDN_FORCE_FFMA if force_ffma else 0) | (GDN_SINGLE_PASS if single_pass else 0)
+    d = make_dims(B, Hk, Hv, S, Dk, Dv, dtype, flags)
+    return int(lib().gdn_prefill_segments(ctypes.byref(d), int(sm_count)))
 
 
 def _conv_call(name, a, weight, b, c, dims, stream):

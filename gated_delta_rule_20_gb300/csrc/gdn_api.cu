@@ -125,6 +125,25 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
     return gdn::launch_decode(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
+int32_t gdn_prefill_segments(const gdn_dims* d, int32_t sm_count) {
+    if (!d || sm_count < 1) return 0;
+    if ((d->dtype != GDN_F32 && d->dtype != GDN_BF16) || (d->flags & ~gdn::kKnownFlags)) return 0;
+    if (d->B < 0 || d->Hk < 1 || d->Hv < 1 || d->S < 0 || d->Dk < 1 || d->Dv < 1 || d->Dk > 128 || d->Dv > 128 ||
+        d->Hv % d->Hk != 0 || d->B * d->Hv > INT32_MAX || d->S > INT32_MAX)
+        return 0;
+    gdn::Problem p{};
+    p.B = (int)d->B;
+    p.Hk = (int)d->Hk;
+    p.Hv = (int)d->Hv;
+    p.S = (int)d->S;
+    p.Dk = (int)d->Dk;
+    p.Dv = (int)d->Dv;
+    p.bf16 = d->dtype == GDN_BF16;
+    p.single_pass = (d->flags & GDN_SINGLE_PASS) != 0;
+    if ((d->flags & GDN_FORCE_FFMA) || !gdn::prefill_tc_supported(p)) return 1;
+    return gdn::prefill_tc_segments(p, sm_count);
+}
+
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims) {
     (void)dims;
     return 0;

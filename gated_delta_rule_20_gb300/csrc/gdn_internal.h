@@ -40,6 +40,9 @@ cudaError_t launch_prefill_ffma(const Problem& p, cudaStream_t stream);
 
 // Chunked prefill on tcgen05 tensor cores (bf16, Dk = Dv = 128).
 bool prefill_tc_supported(const Problem& p);
+// Segments the tensor-core prefill splits each sequence into on a device with `sms` SMs
+// (1: one pass).
+int prefill_tc_segments(const Problem& p, int sms);
 gdn_status launch_prefill_tc(const Problem& p, int* status_word, cudaStream_t stream);
 
 // The conv1d decode step folded into the gated step: q|k|v are computed from the

@@ -1029,6 +1029,11 @@ int split_segments(int heads, int n_chunks, int sms) {
 
 bool prefill_tc_supported(const Problem& p) { return p.bf16 && p.Dk == kD && p.Dv == kD; }
 
+int prefill_tc_segments(const Problem& p, int sms) {
+    if (p.single_pass || p.B == 0 || p.S == 0) return 1;
+    return split_segments(p.B * p.Hv, (p.S + kC - 1) / kC, sms);
+}
+
 gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_t stream) {
     CUtensorMap tq, tk, tv, to;
     if (!encode_bf16_3d(&tq, p.q, p.B * p.Hk, p.S, 64, true) || !encode_bf16_3d(&tk, p.k, p.B * p.Hk, p.S, 64, true) ||
@@ -1071,7 +1076,7 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     PrefillRuns runs{};
     runs.heads = heads;
     const int n_chunks = (p.S + kC - 1) / kC;
-    const int P = p.single_pass ? 1 : split_segments(heads, n_chunks, sm_count[dev]);
+    const int P = prefill_tc_segments(p, sm_count[dev]);
     const size_t hs = (size_t)heads * kD * kD;  // floats in one state per head
     const long long one = (long long)kD * kD;  // floats in one head's state
     void* ws = nullptr;

@@ -301,6 +301,12 @@ gdn_status gdn_prefill_gated(const void* q, const void* k, const void* v, const 
  * allocates its own stream-ordered scratch). */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);
 
+/* Segments gdn_prefill splits each sequence into for these dims on a device
+ * with sm_count SMs (see gdn_prefill): 1 for one pass (every shape off the
+ * tensor-core path, GDN_FORCE_FFMA, GDN_SINGLE_PASS, B == 0 or S == 0),
+ * otherwise 3 .. 17.  0 for invalid dims or sm_count < 1.  Host only. */
+int32_t gdn_prefill_segments(const gdn_dims* dims, int32_t sm_count);
+
 /* Static, NUL-terminated description of a status code. */
 const char* gdn_status_string(gdn_status s);
 
@@ -312,8 +318,9 @@ const char* gdn_status_string(gdn_status s);
  */
 gdn_status gdn_device_status(int device, int clear, int32_t* code);
 
-/* Number of kernels one call of gdn_prefill, gdn_decode_step, gdn_decode_gated or
- * the conv1d entry points launches (one); gdn_decode_block launches three. */
+/* Number of kernels one call of gdn_prefill (in one pass), gdn_decode_step,
+ * gdn_decode_gated or the conv1d entry points launches: one.  A split prefill
+ * launches four, gdn_decode_block and gdn_prefill_gated two. */
 int gdn_kernels_per_call(void);
 
 #ifdef __cplusplus

@@ -92,6 +92,31 @@ def test_empty_batch_is_a_no_op(L):
     assert _call(L, "gdn_decode_step", d) == gdn.GDN_OK
 
 
+def test_prefill_segments():
+    """The split rule of gdn_prefill (host only): at most a third as many sequences as SMs,
+    segments of 8 chunks or more, at most 17; one pass off the tensor-core path or when
+    asked for; 0 for invalid dims."""
+    seg = gdn.prefill_segments
+    assert seg(1, 16, 32, 32768, sm_count=152) == 3       # the long workload: 32 sequences
+    assert seg(4, 16, 32, 4096, sm_count=152) == 1        # 128 sequences: one pass
+    assert seg(1, 1, 2, 32768, sm_count=152) == 17        # capped by the run table
+    assert seg(1, 1, 1, 1536, sm_count=152) == 3          # 24 chunks: three of 8
+    assert seg(1, 1, 1, 1472, sm_count=152) == 1          # 23 chunks
+    assert seg(2, 5, 25, 1536, sm_count=152) == 3         # 50 sequences, 150 CTAs in the first launch
+    assert seg(2, 5, 25, 1536, sm_count=148) == 1         # 3 x 50 > 148
+    assert seg(1, 1, 8, 16384, sm_count=152) == 11
+    assert seg(1, 1, 2, 32768, dtype=gdn.GDN_F32, sm_count=152) == 1
+    assert seg(1, 1, 2, 32768, Dk=64, Dv=64, sm_count=152) == 1
+    assert seg(1, 1, 2, 32768, sm_count=152, single_pass=True) == 1
+    assert seg(1, 1, 2, 32768, sm_count=152, force_ffma=True) == 1
+    assert seg(0, 1, 2, 32768, sm_count=152) == 1 and seg(1, 1, 2, 0, sm_count=152) == 1
+    assert seg(1, 2, 3, 4096, sm_count=152) == 0          # Hv % Hk != 0
+    assert seg(1, 1, 2, 4096, Dk=129, sm_count=152) == 0
+    assert seg(1, 1, 2, 4096, sm_count=0) == 0
+    L = gdn.lib()
+    assert L.gdn_prefill_segments(None, 152) == 0
+
+
 def test_prefill_flags_known(L):
     # every documented flag passes validation (B = 0: no CUDA call); the next bit does not
     for f in (gdn.GDN_ZERO_INITIAL_STATE, gdn.GDN_FORCE_FFMA, gdn.GDN_SINGLE_PASS,

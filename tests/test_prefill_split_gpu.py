@@ -25,17 +25,9 @@ def _status_clean():
     assert gdn.device_status(0, clear=True) == 0, "a kernel reported a wait timeout"
 
 
-def segments(heads, S, sms, max_runs=32):
-    """The segment count gdn_prefill picks (1: one pass); restated from its documented rule."""
-    n = (S + 63) // 64
-    if heads * 3 > sms:
-        return 1
-    P = min((sms - heads) // (2 * heads) + 2, (max_runs + 3) // 2, n // 8)
-    if P < 3:
-        return 1
-    L = (n + P - 1) // P
-    P = (n + L - 1) // L
-    return P if P >= 3 else 1
+def segments(w):
+    """The segment count gdn_prefill picks for workload w on this GPU (1: one pass)."""
+    return gdn.prefill_segments(w.B, w.Hk, w.Hv, w.S)
 
 
 # name, B, Hk, Hv, S, state std, log-decay range, beta std, seed, sampled sequences (None: all)
@@ -78,9 +70,8 @@ def _picks(w, n, seed):
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_split_prefill_matches_oracle(case):
     w, x = _inputs(case)
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
-    if segments(w.B * w.Hv, w.S, sms) < 3:  # every case splits on a 152-SM GB300
-        pytest.skip("not split on a GPU with %d SMs" % sms)
+    if segments(w) < 3:  # every case splits on a 152-SM GB300
+        pytest.skip("not split on this GPU")
     out, st = _run(x)
     picks = _picks(w, case[-1], case[8])
     ro, rs = oracle_for(x, picks, w.Hv // w.Hk)
@@ -97,9 +88,8 @@ def test_split_prefill_agrees_with_one_pass(case):
     assert rel_l2(to64(o1), to64(o2)) < 1e-2
     assert rel_l2(to64(s1), to64(s2)) < 1e-2
     # segment 0 runs from the real start state in both forms, on the same kernel and tokens
-    sms = torch.cuda.get_device_properties(0).multi_processor_count
     n = (w.S + 63) // 64
-    P = segments(w.B * w.Hv, w.S, sms)
+    P = segments(w)
     L = 64 * ((n + P - 1) // P)
     assert torch.equal(o1[:, :, :L], o2[:, :, :L])
 
