@@ -169,3 +169,28 @@ def test_empty_sequence_keeps_state():
     o, s = oracle.recurrence(q, k, v, g, beta, 0.7, st0)
     assert o.shape == (2, 4, 0, 3)
     np.testing.assert_array_equal(s, st0)
+
+
+@pytest.mark.parametrize("g_range", [(-0.5, -0.005), (-1e-4, 0.0)])
+def test_final_state_is_affine_in_the_start_state(g_range):
+    """The fact the split prefill rests on: over a segment, the final state is M S0 + X, with X
+    the final state from a zero start and M the final state from S0 = I with v = 0 (Dk = Dv),
+    for any S0; and the outputs likewise split into a part linear in S0 and the zero-start
+    part.  Checked against the recurrence from random start states, including almost no decay
+    (where M is far from zero)."""
+    rng = np.random.default_rng(23)
+    D = 6
+    q, k, v, g, beta, _ = _rand_inputs(rng, B=1, Hk=1, Hv=2, S=29, Dk=D, Dv=D, state=False,
+                                       g_lo=g_range[0], g_hi=g_range[1])
+    _, X = oracle.recurrence(q, k, v, g, beta, 1.0, None)
+    eye = np.broadcast_to(np.eye(D), (1, 2, D, D)).copy()
+    _, M = oracle.recurrence(q, k, np.zeros_like(v), g, beta, 1.0, eye)
+    o0, _ = oracle.recurrence(q, k, v, g, beta, 1.0, None)
+    oM, _ = oracle.recurrence(q, k, np.zeros_like(v), g, beta, 1.0, eye)
+    assert np.abs(M).max() > 1e-5  # the map is not trivially zero over 29 tokens
+    for _ in range(3):
+        S0 = rng.standard_normal((1, 2, D, D))
+        o, S = oracle.recurrence(q, k, v, g, beta, 1.0, S0)
+        np.testing.assert_allclose(S, np.einsum("bhij,bhjk->bhik", M, S0) + X, rtol=1e-10, atol=1e-12)
+        # out_t = (M_t S0)^T q_t + out_t(zero start); with v = 0 from I the output is (M_t)^T q_t
+        np.testing.assert_allclose(o, np.einsum("bhtj,bhjk->bhtk", oM, S0) + o0, rtol=1e-10, atol=1e-12)
