@@ -289,7 +289,8 @@ __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const C
 // A launch processes up to kMaxRuns runs over the same heads: run r covers tokens
 // t0 .. t0 + len - 1 of every (batch, value head) sequence, CTA blockIdx.x = r * heads + head.
 // A plain prefill is one run over the whole sequence; a split one (host side, below) uses
-// runs over segments, some of them from a zero or identity start.
+// runs over segments, some of them state-only runs from a zero start or from the identity
+// with v = 0.
 struct PrefillRun {
     const float* state_in;  // initial states, head h at state_in + h * in_stride; nullptr: zero
     float* state_out;       // final states [heads, Dk, Dv]; may equal state_in
@@ -1011,7 +1012,7 @@ __global__ void identity_kernel(float* I) { I[blockIdx.x * kD + threadIdx.x] = b
 // Segments for a prefill of `heads` sequences of n_chunks chunks on `sms` SMs (1: no split).
 // A split into P segments runs in two waves of about n_chunks / P chunks: first segment 0
 // from the real start state and, for each middle segment, one run from a zero start and one
-// from the identity (heads * (2P - 3) CTAs, one per SM); then segments 1 .. P - 1 from the
+// from the identity with v = 0 (heads * (2P - 3) CTAs, one per SM); then segments 1 .. P - 1 from the
 // start states the combine kernel derives.  Worth it from P = 3, with segments of at least
 // 8 chunks; 2P - 3 runs must fit one launch.
 int split_segments(int heads, int n_chunks, int sms) {
