@@ -56,6 +56,31 @@ def check(out, state, ref_out, ref_state, bf16, what=""):
     return float(np.abs(o - ref_out).max()), float(np.abs(s - ref_state).max())
 
 
+def check_whole(out, state, ref_out, ref_state, what=""):
+    """bf16 contract over the WHOLE tensors: relative L2 of out and of the final state,
+    each taken over every element of every (batch, value head) sequence.  The worst
+    per-sequence relative L2 is printed as a diagnostic (not asserted: a sequence whose
+    reference output is tiny can have a large relative error that the contract allows)."""
+    o, s = to64(out), to64(state)
+    assert np.isfinite(o).all() and np.isfinite(s).all(), what + ": non-finite values"
+    eo, es = rel_l2(o, ref_out), rel_l2(s, ref_state)
+    n = o.shape[0] * o.shape[1]
+
+    def worst(a, ref):
+        d = np.linalg.norm((a - ref).reshape(n, -1), axis=1)
+        r = np.maximum(np.linalg.norm(np.asarray(ref).reshape(n, -1), axis=1), 1e-300)
+        i = int(np.argmax(d / r))
+        return float(d[i] / r[i]), divmod(i, o.shape[1])
+
+    wo, io = worst(o, ref_out)
+    ws, is_ = worst(s, ref_state)
+    print("%s: %d sequences; out rel L2 %.3e (worst sequence %.3e at (b, h) = %s); "
+          "state rel L2 %.3e (worst %.3e at %s)" % (what, n, eo, wo, io, es, ws, is_))
+    assert eo <= BF16_REL_L2, "%s: out rel L2 %.3e" % (what, eo)
+    assert es <= BF16_REL_L2, "%s: state rel L2 %.3e" % (what, es)
+    return eo, es
+
+
 def run_prefill(x, force_ffma=False, guard=0):
     """Call the library; outputs are pre-filled with NaN so an unwritten element
     shows, and optional guard elements around out and state must stay untouched."""

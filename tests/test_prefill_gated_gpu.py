@@ -75,23 +75,18 @@ def test_prefill_gated(gdn, w):
     assert gdn.device_status(0) == 0
 
 
-def test_prefill_gated_full_size_sampled(gdn):
-    """The bench's size (B=4, Hk=16, Hv=32, S=4096, bf16, tcgen05 path), checked on three
-    sampled (batch, value head) sequences against the oracle."""
-    from gpu_util import sample_heads
+def test_prefill_gated_full_size(gdn):
+    """The bench's size (B=4, Hk=16, Hv=32, S=4096, bf16, tcgen05 path), compared with the
+    oracle over every (batch, value head) sequence: relative L2 over the whole gated output
+    and the whole final state."""
+    from gpu_util import check_whole
     w = workloads.PREFILL
     x = workloads.make_inputs(w, device="cuda")
     gz = workloads.make_gate_inputs(w, device="cuda")
     out, st = gdn.prefill_gated(x["q"], x["k"], x["v"], x["g_log"], x["beta"], gz["z"], gz["norm_weight"],
                                 x["scale"], x["state"].clone())
     torch.cuda.synchronize()
-    heads = [(0, 0), (1, 17), (3, 31)]
-    s = sample_heads(x, heads, w.Hv // w.Hk)
-    zs = torch.stack([gz["z"][b, h] for b, h in heads]).unsqueeze(1)
-    ry, rs = opg.prefill_gated(s["q"], s["k"], s["v"], s["g_log"], s["beta"], zs, gz["norm_weight"], x["scale"],
-                               s["state"])
-    got_y = torch.stack([out[b, h] for b, h in heads]).unsqueeze(1)
-    got_s = torch.stack([st[b, h] for b, h in heads]).unsqueeze(1)
-    _check(got_y, ry, "bf16", "full-size gated prefill out")
-    _check(got_s, rs, "bf16", "full-size gated prefill state")
+    ry, rs = opg.prefill_gated(x["q"], x["k"], x["v"], x["g_log"], x["beta"], gz["z"], gz["norm_weight"], x["scale"],
+                               x["state"])
+    check_whole(out, st, ry, rs, "full-size gated prefill")
     assert gdn.device_status(0) == 0
