@@ -8,6 +8,9 @@
                  q/k, gates from raw inputs, RMSNormGated output (C ABI: ``gdn_decode_gated``)
 ``decode_block``  one token through the decode block without its output projection:
                  input projections, conv1d decode, gated step (C ABI: ``gdn_decode_block``)
+``decode_block_noalloc``  the same block step with its scratch in a fixed array inside the
+                 library, for callers that cannot allocate device memory (C ABI:
+                 ``gdn_decode_block_noalloc``)
 ``rmsnorm_gated`` the RMSNormGated output epilogue over rows (C ABI: ``gdn_rmsnorm_gated``)
 ``prefill_gated`` the prefill with RMSNormGated on every token's output (C ABI: ``gdn_prefill_gated``)
 
@@ -18,13 +21,13 @@ missing library raises.
 from ._binding import (EXPORTED, GDN_BF16, GDN_ERR_ALIGN, GDN_ERR_CUDA, GDN_ERR_DIMS, GDN_ERR_NULL,
                        GDN_ERR_TIMEOUT, GDN_ERR_UNSUPPORTED, GDN_F32, GDN_FORCE_FFMA, GDN_OK, GDN_SINGLE_PASS,
                        GDN_ZERO_INITIAL_STATE, LIB_PATH, GdnBlockDims, GdnConvDims, GdnDims, GdnError, conv1d_decode,
-                       conv1d_prefill, decode_block, decode_block_workspace_bytes, decode_gated, decode_step,
+                       conv1d_prefill, decode_block, decode_block_noalloc, decode_block_workspace_bytes, decode_gated, decode_step,
                        device_status, kernels_per_call, lib, make_dims, prefill, prefill_gated, prefill_segments,
                        rmsnorm_gated,
                        status_string)
 
 __all__ = ["prefill", "prefill_segments", "decode_step", "conv1d_prefill", "conv1d_decode", "decode_gated", "decode_block",
-           "decode_block_workspace_bytes", "rmsnorm_gated", "prefill_gated", "GdnBlockDims", "GdnConvDims",
+           "decode_block_noalloc", "decode_block_workspace_bytes", "rmsnorm_gated", "prefill_gated", "GdnBlockDims", "GdnConvDims",
            "device_status",
            "kernels_per_call", "lib", "make_dims", "status_string", "GdnDims", "GdnError", "EXPORTED", "LIB_PATH", "GDN_OK", "GDN_ERR_NULL", "GDN_ERR_DIMS",
            "GDN_ERR_UNSUPPORTED", "GDN_ERR_ALIGN", "GDN_ERR_CUDA", "GDN_ERR_TIMEOUT", "GDN_F32", "GDN_BF16",

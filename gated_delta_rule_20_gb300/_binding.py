@@ -33,7 +33,7 @@ GDN_SINGLE_PASS = 1 << 2
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
             "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
             "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block", "gdn_rmsnorm_gated",
-            "gdn_prefill_gated", "gdn_prefill_segments")
+            "gdn_prefill_gated", "gdn_prefill_segments", "gdn_decode_block_noalloc")
 
 
 class GdnDims(ctypes.Structure):
@@ -94,6 +94,9 @@ def lib() -> ctypes.CDLL:
         L.gdn_decode_block.restype = ctypes.c_int
         L.gdn_decode_block.argtypes = [vp, vp, vp, vp, vp, fp, vp, fp, fp, fp, fp, vp, vp, ctypes.c_size_t,
                                        ctypes.POINTER(GdnBlockDims), vp]
+        L.gdn_decode_block_noalloc.restype = ctypes.c_int
+        L.gdn_decode_block_noalloc.argtypes = [vp, vp, vp, vp, vp, fp, vp, fp, fp, fp, fp, vp,
+                                               ctypes.POINTER(GdnBlockDims), vp]
         for name in ("gdn_conv1d_prefill", "gdn_conv1d_decode"):
             f = getattr(L, name)
             f.restype = ctypes.c_int
@@ -399,5 +402,35 @@ def decode_block(hidden, W_qkv, W_z, W_a, W_b, conv_weight, conv_state, A_log, d
                                       _ptr(conv_state), _ptr(A_log), _ptr(dt_bias), _ptr(norm_weight), _ptr(state),
                                       _ptr(out), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
                                       ctypes.byref(dims), ctypes.c_void_p(stream.cuda_stream))
+    _check(code)
+    return out, conv_state, state
+
+
+# Bytes of the fixed scratch array gdn_decode_block_noalloc uses (GDN_NOALLOC_SCRATCH_BYTES).
+NOALLOC_SCRATCH_BYTES = 4 << 20
+
+
+def decode_block_noalloc(hidden, W_qkv, W_z, W_a, W_b, conv_weight, conv_state, A_log, dt_bias, norm_weight, state,
+                         Hk, Hv, Dk, Dv, out, *, stream=None):
+    """``gdn_decode_block_noalloc``: one token through the decode block with the inter-stage
+    scratch in the library's fixed array (no workspace, no allocation by the library).
+    ``out`` [B, 1, Hv Dv] bf16 is supplied by the caller; ``conv_state`` and ``state`` are
+    updated in place.  Calls that may overlap on the GPU must be serialised on one stream."""
+    torch = _torch()
+    B, _, H = hidden.shape
+    K = conv_weight.shape[1]
+    dims = GdnBlockDims(B, H, Hk, Hv, Dk, Dv, K, _dtype_code(hidden), 0)
+    for nm, t in (("hidden", hidden), ("W_qkv", W_qkv), ("W_z", W_z), ("W_a", W_a), ("W_b", W_b),
+                  ("conv_weight", conv_weight), ("conv_state", conv_state), ("A_log", A_log), ("dt_bias", dt_bias),
+                  ("norm_weight", norm_weight), ("state", state), ("out", out)):
+        if not t.is_cuda or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous CUDA tensor" % nm)
+    if stream is None:
+        stream = torch.cuda.current_stream(hidden.device)
+    with torch.cuda.device(hidden.device):
+        code = lib().gdn_decode_block_noalloc(_ptr(hidden), _ptr(W_qkv), _ptr(W_z), _ptr(W_a), _ptr(W_b),
+                                              _ptr(conv_weight), _ptr(conv_state), _ptr(A_log), _ptr(dt_bias),
+                                              _ptr(norm_weight), _ptr(state), _ptr(out), ctypes.byref(dims),
+                                              ctypes.c_void_p(stream.cuda_stream))
     _check(code)
     return out, conv_state, state

@@ -379,3 +379,54 @@ extern "C" gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, co
                                 1.0f / std::sqrt((float)d->Dk), state_inout, out, &gd, s, true, &conv,
                                 reinterpret_cast<int*>(ws + L.off_ctr));
 }
+
+// ------------------------------------------------------------------ fixed-scratch variant
+// gdn_decode_block_noalloc: the same two launches, with the inter-stage scratch (z, a, b and
+// the head counter) in a fixed array of this library instead of a caller's workspace, for
+// callers that cannot allocate device memory themselves.  Each CUDA device that loads the
+// library holds its own copy of the array until the process exits.  Host code may not use
+// the array's name as a device address (on the host it names a stand-in object), so its
+// device address is looked up once per device with cudaGetSymbolAddress while that device
+// is current, and handed to the kernels like a workspace pointer.
+static __device__ __align__(256) uint8_t g_block_scratch[GDN_NOALLOC_SCRATCH_BYTES];
+
+namespace gdn {
+namespace {
+constexpr int kScratchDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_addr[kScratchDevices] = {};
+
+// Device address of the current device's scratch array (looked up on the first call per device).
+gdn_status block_scratch_for_current_device(void** out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kScratchDevices) return GDN_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_scratch_mu);
+    if (!g_scratch_addr[dev]) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_block_scratch) != cudaSuccess) {
+            (void)cudaGetLastError();
+            return GDN_ERR_CUDA;
+        }
+        g_scratch_addr[dev] = p;
+    }
+    *out = g_scratch_addr[dev];
+    return GDN_OK;
+}
+}  // namespace
+}  // namespace gdn
+
+extern "C" gdn_status gdn_decode_block_noalloc(const void* hidden, const void* W_qkv, const void* W_z, const void* W_a,
+                                               const void* W_b, const float* conv_weight, void* conv_state_inout,
+                                               const float* A_log, const float* dt_bias, const float* norm_weight,
+                                               float* state_inout, void* out, const gdn_block_dims* d,
+                                               gdn_stream_t stream) {
+    gdn_status st = check_block(d);
+    if (st != GDN_OK || d->B == 0) return st;
+    // z, a, b and the counter must fit the fixed array; the GEMM overwrites z, a and b and
+    // zeroes the counter on every call, so nothing left by an earlier call is read
+    if (layout(d).bytes > GDN_NOALLOC_SCRATCH_BYTES) return GDN_ERR_UNSUPPORTED;
+    void* ws = nullptr;
+    if ((st = block_scratch_for_current_device(&ws)) != GDN_OK) return st;
+    return gdn_decode_block(hidden, W_qkv, W_z, W_a, W_b, conv_weight, conv_state_inout, A_log, dt_bias, norm_weight,
+                            state_inout, out, ws, GDN_NOALLOC_SCRATCH_BYTES, d, stream);
+}

@@ -240,6 +240,9 @@ typedef struct {
     uint32_t flags;  /* 0 */
 } gdn_block_dims;
 
+/* Size of the fixed scratch array that gdn_decode_block_noalloc uses (4 MiB). */
+#define GDN_NOALLOC_SCRATCH_BYTES ((size_t)4 << 20)
+
 /* Device workspace bytes gdn_decode_block needs (the inter-stage activations z,
  * a, b in bf16, and a work counter of the gated step); 0 for invalid dims. */
 size_t gdn_decode_block_workspace_bytes(const gdn_block_dims* dims);
@@ -267,6 +270,38 @@ gdn_status gdn_decode_block(const void* hidden, const void* W_qkv, const void* W
                             const float* A_log, const float* dt_bias, const float* norm_weight,
                             float* state_inout, void* out, void* workspace, size_t workspace_bytes,
                             const gdn_block_dims* dims, gdn_stream_t stream);
+
+/*
+ * gdn_decode_block_noalloc -- gdn_decode_block for callers that cannot allocate
+ * device memory: a runtime that owns every byte of the device and hands out no
+ * buffers to kernels it does not know, a plugin whose host code must not call the
+ * CUDA allocator, or a serving loop that may not risk an allocation (which can
+ * synchronise the device or fail under memory pressure) while it runs.  The
+ * pages' block kernel has no such variant; it exists for this library's callers.
+ *
+ * Arguments and results are those of gdn_decode_block without the workspace: the
+ * inter-stage scratch (z, a, b in bf16 and the gated step's head counter) lives
+ * in a fixed array inside the library, GDN_NOALLOC_SCRATCH_BYTES bytes, of which
+ * every CUDA device that loads the library keeps one copy until the process
+ * exits.  Dims whose scratch, gdn_decode_block_workspace_bytes, exceeds that size
+ * return GDN_ERR_UNSUPPORTED and launch nothing (for the workloads here, B = 64
+ * and value_dim = 4096 need 0.5 MiB; B = 256 with value_dim = 4096 about 2 MiB).
+ * The call allocates nothing: no cudaMalloc, cudaFree or allocating library
+ * routine.
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that first
+ * call before any stream capture on the device.  Every call on a device shares
+ * the one array, and the array keeps the previous call's contents: each call
+ * rewrites z, a and b and clears the counter before reading them, so results do
+ * not depend on earlier calls, but two calls whose kernels overlap on the GPU
+ * (different streams, or different host threads, without ordering between them)
+ * race on the array and give wrong results.  Serialise such calls on one stream.
+ */
+gdn_status gdn_decode_block_noalloc(const void* hidden, const void* W_qkv, const void* W_z, const void* W_a,
+                                    const void* W_b, const float* conv_weight, void* conv_state_inout,
+                                    const float* A_log, const float* dt_bias, const float* norm_weight,
+                                    float* state_inout, void* out, const gdn_block_dims* dims, gdn_stream_t stream);
 
 /*
  * gdn_rmsnorm_gated -- the RMSNormGated output epilogue ("GDN Block TKG Kernel
