@@ -33,7 +33,8 @@ GDN_SINGLE_PASS = 1 << 2
 EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gdn_status_string",
             "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
             "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block", "gdn_rmsnorm_gated",
-            "gdn_prefill_gated", "gdn_prefill_segments", "gdn_decode_block_noalloc")
+            "gdn_prefill_gated", "gdn_prefill_segments", "gdn_decode_block_noalloc",
+            "gdn_set_wait_limit_ns", "gdn_test_stall_prefill")
 
 
 class GdnDims(ctypes.Structure):
@@ -82,6 +83,10 @@ def lib() -> ctypes.CDLL:
         L.gdn_status_string.argtypes = [ctypes.c_int]
         L.gdn_device_status.restype = ctypes.c_int
         L.gdn_device_status.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.POINTER(ctypes.c_int32)]
+        L.gdn_set_wait_limit_ns.restype = ctypes.c_int
+        L.gdn_set_wait_limit_ns.argtypes = [ctypes.c_int, ctypes.c_uint64]
+        L.gdn_test_stall_prefill.restype = ctypes.c_int
+        L.gdn_test_stall_prefill.argtypes = [ctypes.c_int, ctypes.c_int]
         L.gdn_kernels_per_call.restype = ctypes.c_int
         L.gdn_kernels_per_call.argtypes = []
         L.gdn_prefill_segments.restype = ctypes.c_int32
@@ -108,6 +113,18 @@ def lib() -> ctypes.CDLL:
                                         vp]
         _lib = L
     return _lib
+
+
+def set_wait_limit_ns(device: int, ns: int) -> None:
+    """``gdn_set_wait_limit_ns``: the give-up time of the tensor-core prefill's waits on ``device``
+    (0 restores the default second).  Meant for exercising the timeout path."""
+    _check(lib().gdn_set_wait_limit_ns(int(device), int(ns)))
+
+
+def test_stall_prefill(device: int, on: bool) -> None:
+    """``gdn_test_stall_prefill``: while on, each tensor-core prefill CTA waits on a barrier that is
+    never arrived at, so that its wait runs out (a test of the give-up path)."""
+    _check(lib().gdn_test_stall_prefill(int(device), 1 if on else 0))
 
 
 def status_string(code: int) -> str:

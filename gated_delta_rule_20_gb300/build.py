@@ -31,12 +31,9 @@ def nvcc() -> str:
     return cand if os.path.exists(cand) else (shutil.which("nvcc") or "nvcc")
 
 
-def _flags(debug: bool):
-    f = ARCH + ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC,
-                "--expt-relaxed-constexpr", "-Xptxas", "-v" if os.environ.get("GDN_PTXAS_VERBOSE") else "-O3"]
-    if debug:
-        f += ["-DGDN_DEBUG=1"]
-    return f
+def _flags():
+    return ARCH + ["-std=c++17", "-O3", "-lineinfo", "-Xcompiler", "-fPIC", "-I" + INCLUDE, "-I" + CSRC,
+                   "--expt-relaxed-constexpr", "-Xptxas", "-v" if os.environ.get("GDN_PTXAS_VERBOSE") else "-O3"]
 
 
 def _stale(obj: str, src: str) -> bool:
@@ -48,9 +45,9 @@ def _stale(obj: str, src: str) -> bool:
     return any(os.path.getmtime(d) > t for d in deps)
 
 
-def build(verbose: bool = False, debug: bool = False, force: bool = False) -> str:
+def build(verbose: bool = False, force: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
-    flags = _flags(debug)
+    flags = _flags()
     jobs = []
     objs = []
     for s in SOURCES:

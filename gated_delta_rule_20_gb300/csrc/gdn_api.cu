@@ -181,6 +181,26 @@ gdn_status gdn_device_status(int device, int clear, int32_t* code) {
     return s;
 }
 
+gdn_status gdn_set_wait_limit_ns(int device, uint64_t ns) {
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaSetDevice(device) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn_status s = GDN_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess || gdn::set_prefill_tc_wait_limit(ns) != cudaSuccess) s = GDN_ERR_CUDA;
+    cudaSetDevice(prev);
+    return s;
+}
+
+gdn_status gdn_test_stall_prefill(int device, int on) {
+    int prev = 0;
+    if (cudaGetDevice(&prev) != cudaSuccess) return GDN_ERR_CUDA;
+    if (cudaSetDevice(device) != cudaSuccess) return GDN_ERR_CUDA;
+    gdn_status s = GDN_OK;
+    if (cudaDeviceSynchronize() != cudaSuccess || gdn::set_prefill_tc_test_stall(on) != cudaSuccess) s = GDN_ERR_CUDA;
+    cudaSetDevice(prev);
+    return s;
+}
+
 int gdn_kernels_per_call(void) { return 1; }
 
 }  // extern "C"

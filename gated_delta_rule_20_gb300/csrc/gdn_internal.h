@@ -44,6 +44,10 @@ bool prefill_tc_supported(const Problem& p);
 // (1: one pass).
 int prefill_tc_segments(const Problem& p, int sms);
 gdn_status launch_prefill_tc(const Problem& p, int* status_word, cudaStream_t stream);
+// The tensor-core prefill's wait limit on the current device (0: the default second).
+cudaError_t set_prefill_tc_wait_limit(unsigned long long ns);
+// The tensor-core prefill's test hook on the current device (see gdn_test_stall_prefill).
+cudaError_t set_prefill_tc_test_stall(int on);
 
 // The conv1d decode step folded into the gated step: q|k|v are computed from the
 // already shifted windows [B, conv_dim, K] bf16 (the newest token last) and the

@@ -195,6 +195,7 @@ struct Bars {
     uint64_t c1;        // chain: Delta product done
     uint64_t c2;        // chain: state increment done
     uint64_t c3;        // chain: output accumulator done
+    uint64_t stall;     // never arrived on: the test hook's wait (see g_test_stall)
     uint32_t tmem_base;
     int abort;
 };
@@ -305,6 +306,11 @@ struct PrefillRuns {
     int heads;
 };
 
+// Test hook (gdn_test_stall_prefill): when non-zero, each CTA's chain first waits on a barrier
+// that nothing arrives at, so that the wait runs out after the wait limit and the CTA takes its
+// give-up path.  Zero in normal use.
+__device__ int g_test_stall = 0;
+
 // kSplit = false: one run over whole sequences (runs.run[0], t0 = 0, len = S), the
 // instantiation a plain prefill launches; its code is that of a kernel without run tables.
 template <bool kSplit>
@@ -356,6 +362,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->c1, 1);
         mbar_init(&bars->c2, 1);
         mbar_init(&bars->c3, 1);
+        mbar_init(&bars->stall, 1);
         bars->abort = 0;
         fence_mbar_init();
     }
@@ -642,6 +649,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         named_bar_sync(BAR_CHAIN, kChain);
         int issued0 = -1, issued1 = -1, issued2 = -1;  // last chunk whose U/W, first, state products were committed
         bool ok = true;
+        if (*const_cast<volatile int*>(&g_test_stall))  // the test hook: a wait that runs out
+            ok = !named_bar_any(BAR_CHAIN, kChain, !mbar_wait_or_abort(&bars->stall, 0, abort_flag));
         for (int c = 0; c < n_chunks && ok; ++c) {
             const int s = c % kStages;  // input stage
             const int db = c & 1;       // TMEM buffer R_D
@@ -1029,6 +1038,16 @@ int split_segments(int heads, int n_chunks, int sms) {
 }  // namespace
 
 bool prefill_tc_supported(const Problem& p) { return p.bf16 && p.Dk == kD && p.Dv == kD; }
+
+cudaError_t set_prefill_tc_wait_limit(unsigned long long ns) {
+    const unsigned long long v = ns ? ns : 1000000000ull;
+    return cudaMemcpyToSymbol(g_wait_limit_ns, &v, sizeof(v));
+}
+
+cudaError_t set_prefill_tc_test_stall(int on) {
+    const int v = on ? 1 : 0;
+    return cudaMemcpyToSymbol(g_test_stall, &v, sizeof(v));
+}
 
 int prefill_tc_segments(const Problem& p, int sms) {
     if (p.single_pass || p.B == 0 || p.S == 0) return 1;

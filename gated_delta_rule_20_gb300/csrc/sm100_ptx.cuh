@@ -81,13 +81,19 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
 // The thread polls (try_wait without a suspend hint blocks for a short,
 // hardware-chosen time per test): resuming from a suspended try_wait was
 // measured to cost more than the polling does.
+// The limit of these waits, in ns (one copy per translation unit; the tensor-core prefill's copy
+// can be lowered from the host to exercise the give-up path, see gdn_set_wait_limit_ns).  The
+// drains above (mbar_wait) keep their fixed second: they wait for copies and products already
+// in flight, which must land before the CTA exits.
+static __device__ unsigned long long g_wait_limit_ns = 1000000000ull;
 static __device__ __noinline__ bool mbar_wait_or_abort_loop(uint64_t* bar, uint32_t parity, volatile int* abort) {
     const uint64_t t0 = globaltimer_ns();
+    const uint64_t limit = *const_cast<volatile unsigned long long*>(&g_wait_limit_ns);
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if ((i & 15u) == 0) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > 1000000000ull) {
+            if (globaltimer_ns() - t0 > limit) {
                 *abort = 1;
                 return false;
             }

@@ -353,6 +353,32 @@ const char* gdn_status_string(gdn_status s);
  */
 gdn_status gdn_device_status(int device, int clear, int32_t* code);
 
+/*
+ * gdn_set_wait_limit_ns -- the time after which a wait inside the tensor-core
+ * prefill (gdn_prefill on bf16 with Dk = Dv = 128) gives up, on CUDA device
+ * `device`: ns > 0 sets it, 0 restores the default of one second.  A wait that
+ * gives up records GDN_ERR_TIMEOUT in the status word (gdn_device_status), the
+ * CTA's roles stop, every copy and product already in flight is drained (those
+ * drains keep their own one-second bound) and the CTA frees its tensor memory
+ * and exits; the outputs of such a call are undefined.  This exists to exercise
+ * that path without a GPU fault (a limit of a few microseconds makes ordinary
+ * waits run out); it synchronises the device.  The pages define no such knob.
+ * Returns GDN_ERR_CUDA if the device cannot be selected or the value not set.
+ */
+gdn_status gdn_set_wait_limit_ns(int device, uint64_t ns);
+
+/*
+ * gdn_test_stall_prefill -- test hook for the path above, on CUDA device `device`:
+ * while on != 0, every CTA of the tensor-core prefill first waits on a barrier
+ * that nothing arrives at, so that the wait runs out after the wait limit (set
+ * it low with gdn_set_wait_limit_ns) and the call takes its give-up path:
+ * GDN_ERR_TIMEOUT in the status word, nothing computed.  No GPU fault is
+ * involved.  Synchronises the device.  Off by default; the pages define no
+ * such hook.  Returns GDN_ERR_CUDA if the device cannot be selected or the
+ * value not set.
+ */
+gdn_status gdn_test_stall_prefill(int device, int on);
+
 /* Number of kernels one call of gdn_prefill (in one pass), gdn_decode_step,
  * gdn_decode_gated or the conv1d entry points launches: one.  A split prefill
  * launches four, gdn_decode_block and gdn_prefill_gated two. */
