@@ -942,13 +942,13 @@ bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_
 // final state from a zero start, M_j its final state from S0 = I with v = 0.  Each state
 // column evolves on its own: blockIdx.x = head, blockIdx.y = a slice of kCols columns, and
 // the slices exchange nothing.  256 threads, thread t: row t / 2, kCols / 2 columns; plain
-// fp32 FMAs.  M_{j+1} and X_{j+1} reach shared memory by cp.async while step j computes,
-// so each step pays one copy latency at most.
+// fp32 FMAs.  M_{j+1} and this slice of X_{j+1} reach shared memory by cp.async while step j
+// computes, so each step pays one copy latency at most.
 constexpr int kCombStride = kD + 4;  // padded rows of M, 16-byte aligned: the 16 rows a warp reads
                                      // fall on 8 distinct 16-byte bank groups
 template <int kCols>
-constexpr size_t comb_smem() {  // raw M_j, X_j; M_j with padded rows; the S_j and X_j slices
-    return (size_t)(2 * kD * kD + kD * kCombStride + 2 * kD * kCols) * sizeof(float);
+constexpr size_t comb_smem() {  // raw M_j; M_j with padded rows; the S_j slice; the X_j slice (two buffers)
+    return (size_t)(kD * kD + kD * kCombStride + 3 * kD * kCols) * sizeof(float);
 }
 
 template <int kCols>
@@ -956,19 +956,19 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
                                                               float* __restrict__ Sst, int heads, int n_maps) {
     extern __shared__ __align__(16) float csm[];
     float* rawM = csm;                  // [128][128] M_j as copied
-    float* rawX = rawM + kD * kD;       // [128][128] X_j
-    float* sM = rawX + kD * kD;         // [128][129] M_j
+    float* sM = rawM + kD * kD;         // [128][132] M_j
     float* sS = sM + kD * kCombStride;  // [128][kCols] this slice of S_j
-    float* sX = sS + kD * kCols;        // [128][kCols] this slice of X_j
+    float* sXb = sS + kD * kCols;       // [2][128][kCols] this slice of X_j, buffer j % 2
     const int h = blockIdx.x, col0 = blockIdx.y * kCols, t = threadIdx.x;
     const size_t hs = (size_t)kD * kD;
+    constexpr int kVecs = kCols / 4;    // 16-byte pieces of a slice row
     auto copy_maps = [&](int j) {
         const float* Mj = Mg + ((size_t)(j - 1) * heads + h) * hs;
         const float* Xj = X + ((size_t)(j - 1) * heads + h) * hs;
-        for (int i = t; i < kD * kD / 4; i += 256) {
-            cp_async_16(rawM + 4 * i, Mj + 4 * i);
-            cp_async_16(rawX + 4 * i, Xj + 4 * i);
-        }
+        float* sXj = sXb + (j & 1) * kD * kCols;
+        for (int i = t; i < kD * kD / 4; i += 256) cp_async_16(rawM + 4 * i, Mj + 4 * i);
+        for (int i = t; i < kD * kVecs; i += 256)  // only the slice's columns of X_j
+            cp_async_16(sXj + 4 * i, Xj + (size_t)(i / kVecs) * kD + col0 + 4 * (i % kVecs));
         cp_async_commit();
     };
     copy_maps(1);
@@ -977,13 +977,13 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
     constexpr int kPer = kCols / 2;
     const int r = t >> 1, c0 = (t & 1) * kPer;
     for (int j = 1; j <= n_maps; ++j) {
+        const float* sX = sXb + (j & 1) * kD * kCols;
         cp_async_wait_all();
-        __syncthreads();  // M_j, X_j and the S_j slice are in shared memory
+        __syncthreads();  // M_j, the X_j slice and the S_j slice are in shared memory
         for (int i = t; i < kD * kD / 4; i += 256)
             *reinterpret_cast<float4*>(sM + (4 * i / kD) * kCombStride + 4 * i % kD) =
                 reinterpret_cast<const float4*>(rawM)[i];
-        for (int i = t; i < kD * kCols; i += 256) sX[i] = rawX[(i / kCols) * kD + col0 + i % kCols];
-        __syncthreads();  // M_j and the X_j slice are built; the raw buffers are free
+        __syncthreads();  // M_j is built; the raw buffer is free (the X_j slice stays in its buffer)
         if (j < n_maps) copy_maps(j + 1);
         float acc[kPer];
 #pragma unroll

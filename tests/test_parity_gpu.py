@@ -142,6 +142,32 @@ def test_prefill_bf16_strong_decay_and_beta():
     check(out, st, ro, rs, True, "bf16 strong decay")
 
 
+def test_prefill_bf16_decay_beyond_factored_range():
+    """Per-token log-decays of -2..-3.5: a 64-token chunk's decay range exceeds what the factored
+    masks take (125 in log2 units), so every chunk evaluates exp(G_r - G_j) per element."""
+    w = small("bf16", S=256, g=(-3.5, -2.0), bs=2.0, state=0.05, seed=32)
+    x = workloads.make_inputs(w, device=DEV)
+    out, st = run_prefill(x)
+    ro, rs = oracle_for(x)
+    check(out, st, ro, rs, True, "bf16 decay beyond the factored range")
+
+
+def test_prefill_bf16_mixed_factored_and_exact_masks():
+    """Chunks alternate between weak decay (factored masks) and very strong decay (per-element
+    exponentials) inside one sequence, and across heads, with a ragged last chunk."""
+    w = small("bf16", S=330, state=0.05, seed=33)
+    x = workloads.make_inputs(w, device=DEV)
+    gen = torch.Generator().manual_seed(33)
+    g = -(0.005 + 0.5 * torch.rand(x["g_log"].shape, generator=gen))
+    strong = -(2.0 + 1.5 * torch.rand(x["g_log"].shape, generator=gen))
+    chunk = torch.arange(w.S) // 64
+    pick = ((chunk[None, None, :] + torch.arange(w.Hv)[None, :, None]) % 2 == 1).expand_as(g)
+    x["g_log"] = torch.where(pick, strong, g).float().to(DEV)
+    out, st = run_prefill(x)
+    ro, rs = oracle_for(x)
+    check(out, st, ro, rs, True, "bf16 mixed mask forms")
+
+
 def test_prefill_bf16_correlated_keys():
     """Keys that share a common direction make A large and the solve harder."""
     w = small("bf16", S=192, seed=41)
