@@ -16,7 +16,7 @@ What the page fixes (Parameters, Returns, Notes of both entry points):
     conv_state [B, C, K]; the FIR reduces to a K-tap dot product over the
     shifted window, and the new conv_state is that shifted window.
 
-Readings where the page is silent (each listed in the design doc):
+Readings where the page is silent (assumptions, stated here and tested by the pins):
   * tap order is that of a depthwise ``Conv1d`` weight (a cross-correlation):
     weight[c, K - 1] multiplies the current token, weight[c, K - 1 - m] the
     token m steps back;

@@ -11,7 +11,7 @@ CUDA library.
 Steps, in the page's order: the four input projections of the token's hidden
 state (matrix products, a library primitive here), the conv1d decode step on the
 q|k|v channels (``oracle.conv1d``), then the gated single-token step
-(``oracle.gated_decode``).  Readings (listed in the design doc): the weights are
+(``oracle.gated_decode``).  Readings where the page is silent: the weights are
 [H, N] (the page: "== nn.Linear.weight.T"), the projections are exact products
 (the GPU rounds them to bf16, like every inter-stage activation), and the query
 scale is 1 / sqrt(head_k_dim), the page giving no scale argument.

@@ -11,8 +11,8 @@ TEST INFRASTRUCTURE, NOT PRODUCT CODE: only ``tests/``, ``__graft_entry__.smoke(
 and the CPU-baseline leg of ``bench.py`` may use it.  It shares no code with the
 CUDA library.
 
-The page names these inputs but prints no formulas.  The readings (each listed
-in DESIGN.md):
+The page names these inputs but prints no formulas.  The readings (assumptions,
+the plainest ones the names support):
   * q, k: x / sqrt(sum(x^2) + eps_l2) over the head dim, eps_l2 = 1e-6;
   * g = -exp(A_log[h]) * softplus(a[b, h] + dt_bias[h]),  softplus(x) = log(1 + e^x);
   * beta = sigmoid(b[b, h]);

@@ -9,8 +9,9 @@ and the CPU-baseline leg of ``bench.py`` may use it.  It shares no code with the
 CUDA library.
 
 Steps: ``oracle.recurrence`` (the pinned per-token recurrence), then
-``oracle.gated_decode.rms_norm_gated`` on each token's output.  Reading (listed
-in DESIGN.md): the page states the epilogue for the decode block's single token;
+``oracle.gated_decode.rms_norm_gated`` on each token's output.  Reading (an
+assumption where the page is silent): the page states the epilogue for the decode
+block's single token;
 here it is applied to every token of a prefill, with z laid out like the output,
 [B, Hv, S, Dv].
 """
