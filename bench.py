@@ -715,7 +715,9 @@ def run_reference(args):
         times.append(r["seconds"])
         cores = r["cores"]
     sec = statistics.mean(times)
-    value = n_seq * w.S / sec
+    # the metric's tokens are the workload's B * S; a step over n_seq of the B * Hv sequences
+    # covers that fraction of them
+    value = w.B * w.S * (n_seq / total) / sec
     desc = ("%d of %d (batch, value-head) sequences x %d tokens per step, measured (not scaled)"
             % (n_seq, total, w.S))
     return {
