@@ -139,10 +139,10 @@ __global__ void __launch_bounds__(kGThreads, 2)
                 if (!mbar_wait_or_abort(&bars->full[s], (i / stages) & 1, abort_flag)) break;
                 tc_fence_after();
                 const uint32_t st = sbase + s * args.stage_bytes;
+                const uint64_t dw = make_sdesc(st, kBoxBytes, 1024), dx = make_sdesc(st + 2 * kBoxBytes, 16, 1024);
 #pragma unroll
                 for (int kk = 0; kk < kSlab / 16; ++kk)
-                    mma_bf16(tmem, make_sdesc(st + kk * 2048, kBoxBytes, 1024),
-                             make_sdesc(st + 2 * kBoxBytes + kk * 32, 16, 1024), args.idesc, (i > 0 || kk > 0));
+                    mma_bf16(tmem, sdesc_add(dw, kk * 2048), sdesc_add(dx, kk * 32), args.idesc, (i > 0 || kk > 0));
                 mma_commit(&bars->empty[s]);
                 issued = i + 1;
             }

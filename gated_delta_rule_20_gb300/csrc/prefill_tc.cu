@@ -392,12 +392,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Gram product [Q; K] K^T of chunk cc into R_G (issued once the chunk has landed)
         auto issue_gram = [&](int cc) {
             const uint32_t st_c = sbase + (cc % kStages) * STAGE_BYTES;
+            const uint64_t da = make_sdesc(st_c + ST_Q0, 16, 1024), dbk = make_sdesc(st_c + ST_K0, 16, 1024);
             tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 const uint32_t off = (kk >> 2) * ST_HALF + (kk & 3) * 32;
-                mma_bf16(tmem + COL_G, make_sdesc(st_c + ST_Q0 + off, 16, 1024),
-                         make_sdesc(st_c + ST_K0 + off, 16, 1024), IDESC_N64_KK, kk > 0);
+                mma_bf16(tmem + COL_G, sdesc_add(da, off), sdesc_add(dbk, off), IDESC_N64_KK, kk > 0);
             }
             mma_commit(&bars->gram);
         };
@@ -664,14 +664,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!fail && c >= 2) fail = !mbar_wait_or_abort(&bars->dfree[db], ((c - 2) >> 1) & 1, abort_flag);
                 if (!fail) {
                     tc_fence_after();
+                    const uint64_t dv = make_sdesc(st_s + ST_VW0, ST_HALF, 1024), dk = make_sdesc(st_s + ST_K0, ST_HALF, 1024);
+                    const uint64_t dt = make_sdesc(sbase + OFF_T12, 16, 1024);
+                    const uint32_t d = tmem + COL_D + 128 * db;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + COL_D + 128 * db, make_sdesc(st_s + ST_VW0 + kk * 2048, ST_HALF, 1024),
-                                 make_sdesc(sbase + OFF_T12 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+                        mma_bf16(d, sdesc_add(dv, kk * 2048), sdesc_add(dt, kk * 32), IDESC_N64_MK, kk > 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(tmem + COL_D + 128 * db + 64, make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024),
-                                 make_sdesc(sbase + OFF_T12 + 8192 + kk * 32, 16, 1024), IDESC_N64_MK, kk > 0);
+                        mma_bf16(d + 64, sdesc_add(dk, kk * 2048), sdesc_add(dt, 8192 + kk * 32), IDESC_N64_MK, kk > 0);
                     mma_commit(&bars->prep_mma[db]);
                     issued0 = c;
                 }
@@ -684,11 +685,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 // [Delta^T | O^T] += S0^T [-W; Q']^T: Delta^T = U^T - S0^T W^T, O^T = S0^T Q'^T
                 // (A = the bf16 state in TMEM, 8 columns per 16-wide K step)
+                const uint64_t dw = make_sdesc(st_s + ST_VW0, 16, 1024);
+                const uint32_t d = tmem + COL_D + 128 * db, a = tmem + COL_SA;
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16_tmem_a(tmem + COL_D + 128 * db, tmem + COL_SA + 8 * kk,
-                                    make_sdesc(st_s + ST_VW0 + (kk >> 2) * ST_HALF + (kk & 3) * 32, 16, 1024),
-                                    IDESC_N128_KK, 1);
+                    mma_bf16_tmem_a(d, a + 8 * kk, sdesc_add(dw, (kk >> 2) * ST_HALF + (kk & 3) * 32), IDESC_N128_KK, 1);
                 mma_commit(&bars->c1);
             }
             issued1 = c;
@@ -740,10 +741,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars->dt_ready);  // the helper warps issue the output product
                 tc_fence_after();
                 // S^T += (Delta^T diag(exp(G_C - G))) K  (A from TMEM)
+                const uint64_t dk = make_sdesc(st_s + ST_K0, ST_HALF, 1024);
+                const uint32_t a = tmem + COL_SA;
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk)
-                    mma_bf16_tmem_a(tmem + COL_S, tmem + COL_SA + 8 * kk,
-                                    make_sdesc(st_s + ST_K0 + kk * 2048, ST_HALF, 1024), IDESC_N128_KM, 1);
+                    mma_bf16_tmem_a(tmem + COL_S, a + 8 * kk, sdesc_add(dk, kk * 2048), IDESC_N128_KM, 1);
                 mma_commit(&bars->c2);
             }
             issued2 = c;
@@ -832,10 +834,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                 fail = !mbar_wait_or_abort(&bars->dt_ready, p & 1, abort_flag);
                 if (!fail && ht == 0) {
                     tc_fence_after();
+                    const uint64_t dp = make_sdesc(st_p + ST_P, 16, 1024);
+                    const uint32_t d = tmem + COL_D + 128 * dbp + 64, a = tmem + COL_D + 128 * dbp;
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_tmem_a(tmem + COL_D + 128 * dbp + 64, tmem + COL_D + 128 * dbp + 8 * kk,
-                                        make_sdesc(st_p + ST_P + kk * 32, 16, 1024), IDESC_N64_KK, 1);
+                        mma_bf16_tmem_a(d, a + 8 * kk, sdesc_add(dp, kk * 32), IDESC_N64_KK, 1);
                     mma_commit(&bars->c3);
                     issued3 = p;
                 }

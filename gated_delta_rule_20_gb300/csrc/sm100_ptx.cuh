@@ -321,6 +321,13 @@ __device__ __forceinline__ uint64_t make_sdesc(uint32_t saddr, uint32_t lbo, uin
     return d;
 }
 
+// The descriptor of the same operand `bytes` further on (a multiple of 16): the start-address
+// field is the low 14 bits of address >> 4 and shared memory stays below 256 KB, so the add
+// never carries out of the field.  A run of MMAs issued from one base descriptor plus
+// constants issues in about 60 cycles per MMA; descriptors rebuilt from a runtime address
+// for every MMA measured about twice that.
+__device__ __forceinline__ uint64_t sdesc_add(uint64_t d, uint32_t bytes) { return d + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 accumulator.
 // a_mn / b_mn select MN-major (1) or K-major (0) operands.
 __host__ __device__ constexpr uint32_t make_idesc_bf16(int M, int N, int a_mn, int b_mn) {
