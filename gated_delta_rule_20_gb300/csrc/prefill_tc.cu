@@ -191,7 +191,7 @@ struct Bars {
     uint64_t dt_ready;        // chain -> helpers: chunk c's Delta^T operands written
     uint64_t req_l2;          // prep -> chain: chunk c's T diag(beta), T diag(beta gamma) written
     uint64_t gram;      // prep: Gram product of a chunk done
-    uint64_t prep_mma[2];  // U, W products of chunk c done, slot c % 2 (waited by the chain and by prep)
+    uint64_t prep_mma[2];  // U, W products of chunk c done, slot c % 2 (two commits; waited by the helpers and by prep)
     uint64_t c1;        // chain: Delta product done
     uint64_t c2;        // chain: state increment done
     uint64_t c3;        // chain: output accumulator done
@@ -358,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(&bars->dt_ready, 1);
         mbar_init(&bars->req_l2, 1);
         mbar_init(&bars->gram, 1);
-        for (int b = 0; b < 2; ++b) mbar_init(&bars->prep_mma[b], 1);
+        for (int b = 0; b < 2; ++b) mbar_init(&bars->prep_mma[b], 2);
         mbar_init(&bars->c1, 1);
         mbar_init(&bars->c2, 1);
         mbar_init(&bars->c3, 1);
@@ -656,23 +656,21 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int db = c & 1;       // TMEM buffer R_D
             const uint32_t st_s = sbase + s * STAGE_BYTES;
             bool fail = false;
-            if (ct == 0) {
-                // ---- [U^T | W^T] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T] into R_D[db], once
-                //      prep has written the solve's operands and the helpers have read chunk c - 2's
-                //      output from that buffer (issued here: this thread waits for its result anyway)
+            if (ct == 0 || ct == 32) {
+                // ---- [U^T | W^T] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T] into R_D[db], U by
+                //      thread 0 and W by thread 32 (two issuers halve the issue time), once prep has
+                //      written the solve's operands and the helpers have read chunk c - 2's output
+                //      from that buffer
                 fail = !mbar_wait_or_abort(&bars->req_l2, c & 1, abort_flag);
                 if (!fail && c >= 2) fail = !mbar_wait_or_abort(&bars->dfree[db], ((c - 2) >> 1) & 1, abort_flag);
                 if (!fail) {
                     tc_fence_after();
-                    const uint64_t dv = make_sdesc(st_s + ST_VW0, ST_HALF, 1024), dk = make_sdesc(st_s + ST_K0, ST_HALF, 1024);
-                    const uint64_t dt = make_sdesc(sbase + OFF_T12, 16, 1024);
-                    const uint32_t d = tmem + COL_D + 128 * db;
+                    const uint64_t da = make_sdesc(st_s + (ct ? ST_K0 : ST_VW0), ST_HALF, 1024);
+                    const uint64_t dt = make_sdesc(sbase + OFF_T12 + (ct ? 8192 : 0), 16, 1024);
+                    const uint32_t d = tmem + COL_D + 128 * db + (ct ? 64 : 0);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(d, sdesc_add(dv, kk * 2048), sdesc_add(dt, kk * 32), IDESC_N64_MK, kk > 0);
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16(d + 64, sdesc_add(dk, kk * 2048), sdesc_add(dt, 8192 + kk * 32), IDESC_N64_MK, kk > 0);
+                        mma_bf16(d, sdesc_add(da, kk * 2048), sdesc_add(dt, kk * 32), IDESC_N64_MK, kk > 0);
                     mma_commit(&bars->prep_mma[db]);
                     issued0 = c;
                 }
@@ -789,6 +787,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int j = 0; j < 32; ++j) Sg[(size_t)(c0 + j) * kD + ct] = x[j];
             }
         }
+        if (ct == 32 && issued0 >= 0) (void)mbar_wait(&bars->prep_mma[issued0 & 1], (issued0 >> 1) & 1);
         if (ct == 0) {  // drain what we issued (bounded; a completed phase returns at once)
             if (issued0 >= 0) (void)mbar_wait(&bars->prep_mma[issued0 & 1], (issued0 >> 1) & 1);
             if (issued1 >= 0) (void)mbar_wait(&bars->c1, issued1 & 1);
@@ -1057,7 +1056,18 @@ int prefill_tc_segments(const Problem& p, int sms) {
     return split_segments(p.B * p.Hv, (p.S + kC - 1) / kC, sms);
 }
 
-gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_t stream) {
+// Split scratch: S_1 .. S_{P-1}, X_1 .. X_{P-2}, M_1 .. M_{P-2} (one state per head each), one
+// identity and one zero v tile [64 tokens][128] bf16.
+constexpr size_t kZeroTile = (size_t)kC * kD * 2;
+size_t prefill_tc_workspace_bytes(const Problem& p, int sms) {
+    const int P = prefill_tc_segments(p, sms);
+    if (P <= 1) return 0;
+    const size_t hs = (size_t)p.B * p.Hv * kD * kD;
+    return ((size_t)(3 * P - 5) * hs + (size_t)kD * kD) * sizeof(float) + kZeroTile;
+}
+
+gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_t stream, void* workspace,
+                             size_t workspace_bytes) {
     CUtensorMap tq, tk, tv, to;
     if (!encode_bf16_3d(&tq, p.q, p.B * p.Hk, p.S, 64, true) || !encode_bf16_3d(&tk, p.k, p.B * p.Hk, p.S, 64, true) ||
         !encode_bf16_3d(&tv, p.v, p.B * p.Hv, p.S, 64, true) ||
@@ -1102,14 +1112,20 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     const int P = prefill_tc_segments(p, sm_count[dev]);
     const size_t hs = (size_t)heads * kD * kD;  // floats in one state per head
     const long long one = (long long)kD * kD;  // floats in one head's state
+    // the split's scratch: the caller's workspace, else stream-ordered memory
     void* ws = nullptr;
-    // stream-ordered scratch: S_1 .. S_{P-1}, X_1 .. X_{P-2}, M_1 .. M_{P-2}, one identity and
-    // one zero v tile [64 tokens][128] bf16
-    constexpr size_t kZeroTile = (size_t)kC * kD * 2;
-    if (P > 1 &&
-        cudaMallocAsync(&ws, ((size_t)(3 * P - 5) * hs + one) * sizeof(float) + kZeroTile, stream) != cudaSuccess) {
-        (void)cudaGetLastError();
-        ws = nullptr;
+    bool own = false;
+    if (P > 1) {
+        const size_t need = prefill_tc_workspace_bytes(p, sm_count[dev]);
+        if (workspace) {
+            if (workspace_bytes < need) return GDN_ERR_WORKSPACE;
+            ws = workspace;
+        } else if (cudaMallocAsync(&ws, need, stream) == cudaSuccess) {
+            own = true;
+        } else {
+            (void)cudaGetLastError();
+            ws = nullptr;
+        }
     }
     if (!ws) {  // one run over the whole sequence
         runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S, 1, 0};
@@ -1146,7 +1162,7 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
         }
         ok = launch(runs, P - 1);
     }
-    ok = cudaFreeAsync(ws, stream) == cudaSuccess && ok;
+    if (own) ok = cudaFreeAsync(ws, stream) == cudaSuccess && ok;
     return ok ? GDN_OK : GDN_ERR_CUDA;
 }
 
