@@ -545,11 +545,14 @@ def run_ours(args, rank, world, local_rank):
     xl = workloads.make_inputs(wl, device=dev)
     lout = torch.empty((wl.B, wl.Hv, wl.S, wl.Dv), dtype=wl.torch_dtype, device=dev)
     lbytes, lflops = prefill_bytes(wl), prefill_flops(wl)
+    # the split's scratch is the caller's (gdn_prefill_ws): the timed region allocates nothing
+    lws_bytes = gdn.prefill_workspace_bytes(wl.B, wl.Hk, wl.Hv, wl.S, wl.Dk, wl.Dv)
+    lws = torch.empty(max(lws_bytes, 16), dtype=torch.uint8, device=dev)
 
     def long_leg(single_pass):
         def step():
             gdn.prefill(xl["q"], xl["k"], xl["v"], xl["g_log"], xl["beta"], xl["scale"], None, lout,
-                        single_pass=single_pass, stream=stream)
+                        single_pass=single_pass, stream=stream, workspace=lws)
         for _ in range(3):
             step()
         torch.cuda.synchronize()
@@ -568,10 +571,12 @@ def run_ours(args, rank, world, local_rank):
 
     long_prefill = {"workload": wl.name, "split": long_leg(False), "single_pass": long_leg(True),
                     "algorithmic_bytes": lbytes, "algorithmic_flops": lflops,
+                    "workspace_bytes": lws_bytes,
                     "note": "split: segment 0 and two state-only runs per middle segment, a combine step, "
                             "then the remaining segments (2 prefill launches, an identity fill and the "
-                            "combine); inputs larger than L2"}
-    del xl, lout
+                            "combine), scratch in a caller workspace allocated before timing; inputs larger "
+                            "than L2"}
+    del xl, lout, lws
 
     # ---------------- wide-GQA batched prefill (B=16, Hk=8, Hv=32, S=2048: 512 sequences, 4 value heads
     #                  per key head), supplied state aliased in and out, inputs larger than L2

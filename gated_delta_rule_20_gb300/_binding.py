@@ -21,6 +21,7 @@ GDN_ERR_UNSUPPORTED = 3
 GDN_ERR_ALIGN = 4
 GDN_ERR_CUDA = 5
 GDN_ERR_TIMEOUT = 6
+GDN_ERR_WORKSPACE = 7
 
 GDN_F32 = 0
 GDN_BF16 = 1
@@ -34,7 +35,7 @@ EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gd
             "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
             "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block", "gdn_rmsnorm_gated",
             "gdn_prefill_gated", "gdn_prefill_segments", "gdn_decode_block_noalloc",
-            "gdn_set_wait_limit_ns", "gdn_test_stall_prefill")
+            "gdn_set_wait_limit_ns", "gdn_test_stall_prefill", "gdn_prefill_ws")
 
 
 class GdnDims(ctypes.Structure):
@@ -77,6 +78,8 @@ def lib() -> ctypes.CDLL:
             f = getattr(L, name)
             f.restype = ctypes.c_int
             f.argtypes = sig
+        L.gdn_prefill_ws.restype = ctypes.c_int
+        L.gdn_prefill_ws.argtypes = sig[:-1] + [vp, ctypes.c_size_t, vp]
         L.gdn_prefill_workspace_bytes.restype = ctypes.c_size_t
         L.gdn_prefill_workspace_bytes.argtypes = [ctypes.POINTER(GdnDims)]
         L.gdn_status_string.restype = ctypes.c_char_p
@@ -158,7 +161,8 @@ def _ptr(t):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, force_ffma, stream, single_pass=False):
+def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, force_ffma, stream, single_pass=False,
+          workspace=None):
     torch = _torch()
     for nm, t in (("q", q), ("k", k), ("v", v), ("g_log", g_log), ("beta", beta), ("state", state), ("out", out)):
         if not t.is_cuda:
@@ -183,20 +187,29 @@ def _call(name, q, k, v, g_log, beta, scale, state, out, zero_initial_state, for
     dims = make_dims(B, Hk, Hv, S, Dk, Dv, dt, flags)
     if stream is None:
         stream = torch.cuda.current_stream(q.device)
+    args = [_ptr(q), _ptr(k), _ptr(v), _ptr(g_log), _ptr(beta), ctypes.c_float(scale), _ptr(state), _ptr(out),
+            ctypes.byref(dims)]
+    if workspace is not None:  # gdn_prefill_ws: a device buffer of workspace.numel() bytes
+        if not workspace.is_cuda or workspace.dtype != torch.uint8 or not workspace.is_contiguous():
+            raise ValueError("workspace must be a contiguous uint8 CUDA tensor")
+        name = "gdn_prefill_ws"
+        args += [_ptr(workspace), ctypes.c_size_t(workspace.numel())]
     with torch.cuda.device(q.device):
-        code = getattr(lib(), name)(_ptr(q), _ptr(k), _ptr(v), _ptr(g_log), _ptr(beta), ctypes.c_float(scale),
-                                    _ptr(state), _ptr(out), ctypes.byref(dims), ctypes.c_void_p(stream.cuda_stream))
+        code = getattr(lib(), name)(*args, ctypes.c_void_p(stream.cuda_stream))
     _check(code)
     return out, state
 
 
-def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=False, single_pass=False, stream=None):
+def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=False, single_pass=False, stream=None,
+            workspace=None):
     """Chunked prefill (``gdn_prefill``).
 
     ``state`` [B,Hv,Dk,Dv] fp32 is updated in place and returned; ``None`` means
     the zero-start form (a new zero-initialised tensor receives the final
     state).  ``single_pass`` sets ``GDN_SINGLE_PASS`` (no split into segments).
-    Returns ``(out, state)``.
+    ``workspace``: a uint8 CUDA tensor of at least ``prefill_workspace_bytes``
+    bytes for a split's scratch (``gdn_prefill_ws``), so that the call allocates
+    nothing.  Returns ``(out, state)``.
     """
     torch = _torch()
     B, Hk, S, Dk = q.shape
@@ -206,7 +219,14 @@ def prefill(q, k, v, g_log, beta, scale, state=None, out=None, *, force_ffma=Fal
         state = torch.empty((B, Hv, Dk, Dv), dtype=torch.float32, device=q.device)
     if out is None:
         out = torch.empty((B, Hv, S, Dv), dtype=q.dtype, device=q.device)
-    return _call("gdn_prefill", q, k, v, g_log, beta, scale, state, out, zero, force_ffma, stream, single_pass)
+    return _call("gdn_prefill", q, k, v, g_log, beta, scale, state, out, zero, force_ffma, stream, single_pass,
+                 workspace)
+
+
+def prefill_workspace_bytes(B, Hk, Hv, S, Dk, Dv, dtype=GDN_BF16, *, force_ffma=False, single_pass=False) -> int:
+    """``gdn_prefill_workspace_bytes`` on the current CUDA device (0 for one pass or without a device)."""
+    flags = (GDN_FORCE_FFMA if force_ffma else 0) | (GDN_SINGLE_PASS if single_pass else 0)
+    return int(lib().gdn_prefill_workspace_bytes(ctypes.byref(make_dims(B, Hk, Hv, S, Dk, Dv, dtype, flags))))
 
 
 def rmsnorm_gated(x, z, norm_weight, out=None, *, stream=None):

@@ -97,21 +97,28 @@ gdn_status prefill_checked(const void* q, const void* k, const void* v, const fl
 
 extern "C" {
 
-gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
-                       float scale, float* state_inout, void* out, const gdn_dims* dims, gdn_stream_t stream) {
+gdn_status gdn_prefill_ws(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
+                          float scale, float* state_inout, void* out, const gdn_dims* dims, void* workspace,
+                          size_t workspace_bytes, gdn_stream_t stream) {
     gdn::Problem p{};
     p.scale = scale;
     gdn_status s = gdn::check(q, k, v, g_log, beta, state_inout, out, dims, false, &p);
     if (s != GDN_OK) return s;
+    if (workspace && gdn::misaligned(workspace)) return GDN_ERR_ALIGN;
     cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (p.B == 0 || p.S == 0) return gdn::empty_sequence(p, st);
     if (!(dims->flags & GDN_FORCE_FFMA) && gdn::prefill_tc_supported(p)) {
         int32_t* status = nullptr;
         s = gdn::status_word_for_current_device(&status);
         if (s != GDN_OK) return s;
-        return gdn::launch_prefill_tc(p, status, st);
+        return gdn::launch_prefill_tc(p, status, st, workspace, workspace_bytes);
     }
     return gdn::launch_prefill_ffma(p, st) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
+}
+
+gdn_status gdn_prefill(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
+                       float scale, float* state_inout, void* out, const gdn_dims* dims, gdn_stream_t stream) {
+    return gdn_prefill_ws(q, k, v, g_log, beta, scale, state_inout, out, dims, nullptr, 0, stream);
 }
 
 gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const float* g_log, const float* beta,
@@ -145,8 +152,23 @@ int32_t gdn_prefill_segments(const gdn_dims* d, int32_t sm_count) {
 }
 
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims) {
-    (void)dims;
-    return 0;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (gdn_prefill_segments(dims, sms) <= 1) return 0;  // also 0 for invalid dims
+    gdn::Problem p{};
+    p.B = (int)dims->B;
+    p.Hk = (int)dims->Hk;
+    p.Hv = (int)dims->Hv;
+    p.S = (int)dims->S;
+    p.Dk = (int)dims->Dk;
+    p.Dv = (int)dims->Dv;
+    p.bf16 = dims->dtype == GDN_BF16;
+    p.single_pass = (dims->flags & GDN_SINGLE_PASS) != 0;
+    return gdn::prefill_tc_workspace_bytes(p, sms);
 }
 
 const char* gdn_status_string(gdn_status s) {
@@ -158,6 +180,7 @@ const char* gdn_status_string(gdn_status s) {
         case GDN_ERR_ALIGN: return "GDN_ERR_ALIGN: a tensor pointer is not 16-byte aligned";
         case GDN_ERR_CUDA: return "GDN_ERR_CUDA: a CUDA call failed";
         case GDN_ERR_TIMEOUT: return "GDN_ERR_TIMEOUT: a kernel wait ran past its bound";
+        case GDN_ERR_WORKSPACE: return "GDN_ERR_WORKSPACE: the workspace is smaller than gdn_prefill_workspace_bytes";
     }
     return "unknown gdn_status";
 }

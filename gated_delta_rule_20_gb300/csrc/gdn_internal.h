@@ -43,7 +43,14 @@ bool prefill_tc_supported(const Problem& p);
 // Segments the tensor-core prefill splits each sequence into on a device with `sms` SMs
 // (1: one pass).
 int prefill_tc_segments(const Problem& p, int sms);
-gdn_status launch_prefill_tc(const Problem& p, int* status_word, cudaStream_t stream);
+// Device scratch of launch_prefill_tc on a device with `sms` SMs: the segment states and maps
+// of a split (0 for one pass).
+size_t prefill_tc_workspace_bytes(const Problem& p, int sms);
+// workspace == nullptr: a split takes stream-ordered scratch itself (and runs one pass if it
+// cannot be had); otherwise the caller's buffer of workspace_bytes >=
+// prefill_tc_workspace_bytes(p, SM count) bytes, 16-byte aligned, is used.
+gdn_status launch_prefill_tc(const Problem& p, int* status_word, cudaStream_t stream, void* workspace,
+                             size_t workspace_bytes);
 // The tensor-core prefill's wait limit on the current device (0: the default second).
 cudaError_t set_prefill_tc_wait_limit(unsigned long long ns);
 // The tensor-core prefill's test hook on the current device (see gdn_test_stall_prefill).

@@ -46,7 +46,8 @@ typedef enum {
     GDN_ERR_UNSUPPORTED = 3, /* allowed by the pages but not implemented by this build      */
     GDN_ERR_ALIGN = 4,       /* a tensor pointer is not 16-byte aligned                     */
     GDN_ERR_CUDA = 5,        /* a CUDA call (launch, attribute, tensor-map encode) failed    */
-    GDN_ERR_TIMEOUT = 6      /* a kernel wait ran past its bound (device status only)        */
+    GDN_ERR_TIMEOUT = 6,     /* a kernel wait ran past its bound (device status only)        */
+    GDN_ERR_WORKSPACE = 7    /* a caller workspace smaller than the call needs              */
 } gdn_status;
 
 /* Compute dtype = dtype of q, k, v and out ("GDN CTE Kernel API Reference",
@@ -331,10 +332,28 @@ gdn_status gdn_prefill_gated(const void* q, const void* k, const void* v, const 
                              const void* z, const float* norm_weight, float scale, float* state_inout, void* out,
                              const gdn_dims* dims, gdn_stream_t stream);
 
-/* Device workspace the caller must supply to gdn_prefill for these dims:
- * always 0 (the single pass keeps its intermediates on chip; a split prefill
- * allocates its own stream-ordered scratch). */
+/* Device scratch a prefill with these dims needs on the current device: the
+ * segment states and maps of a split (see gdn_prefill; the split depends on
+ * the device's SM count), 0 when the call runs one pass.  0 as well for
+ * invalid dims or when no CUDA device can be queried.  Host only. */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);
+
+/*
+ * gdn_prefill_ws -- gdn_prefill with the scratch of a split supplied by the
+ * caller.  No counterpart on the pages (their kernels allocate nothing the
+ * caller sees); it exists so that a split prefill need not allocate.
+ *   workspace        device memory of workspace_bytes >= gdn_prefill_workspace_bytes(dims)
+ *                    bytes on the current device, 16-byte aligned, owned by the caller
+ *                    and not touched by anything else until the call's work on `stream`
+ *                    has finished; NULL: the call behaves exactly like gdn_prefill
+ *                    (stream-ordered scratch of its own)
+ * A non-NULL workspace that is too small returns GDN_ERR_WORKSPACE (misaligned:
+ * GDN_ERR_ALIGN) and launches nothing.  Results are bit-identical to gdn_prefill's.
+ */
+gdn_status gdn_prefill_ws(const void* q, const void* k, const void* v,
+                          const float* g_log, const float* beta, float scale,
+                          float* state_inout, void* out, const gdn_dims* dims,
+                          void* workspace, size_t workspace_bytes, gdn_stream_t stream);
 
 /* Segments gdn_prefill splits each sequence into for these dims on a device
  * with sm_count SMs (see gdn_prefill): 1 for one pass (every shape off the

@@ -6,6 +6,7 @@ import os
 import re
 
 import pytest
+import torch
 
 import gated_delta_rule_20_gb300 as gdn
 from gated_delta_rule_20_gb300 import build as gbuild
@@ -37,16 +38,33 @@ def test_library_exports_every_declared_symbol(L):
 
 
 def test_status_strings(L):
-    for code in range(7):
+    for code in range(8):
         s = gdn.status_string(code)
         assert s.startswith("GDN_"), s
     assert "unknown" in gdn.status_string(99)
 
 
-def test_workspace_is_zero(L):
-    d = gdn.make_dims(4, 16, 32, 4096, 128, 128, gdn.GDN_BF16)
-    assert L.gdn_prefill_workspace_bytes(ctypes.byref(d)) == 0
+def test_workspace_query_without_a_device(L):
+    # the split's scratch depends on the device's SM count: with no device to query, 0
+    d = gdn.make_dims(1, 16, 32, 32768, 128, 128, gdn.GDN_BF16)
+    if not torch.cuda.is_available():
+        assert L.gdn_prefill_workspace_bytes(ctypes.byref(d)) == 0
+    assert L.gdn_prefill_workspace_bytes(None) == 0
     assert gdn.kernels_per_call() == 1
+
+
+def test_prefill_ws_argument_checks(L):
+    def call(dims, ws, nbytes, state=16):
+        p = ctypes.c_void_p(16)
+        return L.gdn_prefill_ws(p, p, p, p, p, ctypes.c_float(1.0), ctypes.c_void_p(state), p,
+                                ctypes.byref(dims) if dims is not None else None,
+                                ctypes.c_void_p(ws) if ws is not None else None, ctypes.c_size_t(nbytes), None)
+    good = gdn.make_dims(1, 1, 2, 256, 128, 128, gdn.GDN_BF16)
+    assert call(None, 4096, 4096) == gdn.GDN_ERR_NULL
+    assert call(gdn.make_dims(1, 2, 3, 256, 128, 128, gdn.GDN_BF16), 4096, 4096) == gdn.GDN_ERR_DIMS
+    assert call(good, 4096, 4096, state=None) == gdn.GDN_ERR_NULL
+    # a misaligned workspace is refused before anything runs (B = 0 would otherwise be a no-op)
+    assert call(gdn.make_dims(0, 1, 2, 256, 128, 128, gdn.GDN_BF16), 4104, 4096) == gdn.GDN_ERR_ALIGN
 
 
 def _call(L, name, dims, ptr=16, state=16):

@@ -138,3 +138,30 @@ def test_split_prefill_graph_replay():
         g.replay()
         torch.cuda.synchronize()
         assert torch.equal(out, o_ref) and torch.equal(st, s_ref)
+
+
+def test_caller_workspace_matches_own_scratch():
+    """gdn_prefill_ws: a split prefill with the caller's scratch gives bit-identical results, a
+    one-pass shape needs none, and a workspace one 16-byte step too small is refused before
+    anything runs."""
+    w = workloads.LONG_PREFILL.with_(S=8192, seed=31)
+    assert segments(w) > 1
+    need = gdn.prefill_workspace_bytes(w.B, w.Hk, w.Hv, w.S, w.Dk, w.Dv)
+    P = segments(w)
+    assert need == ((3 * P - 5) * w.B * w.Hv * 128 * 128 + 128 * 128) * 4 + 64 * 128 * 2
+    assert gdn.prefill_workspace_bytes(w.B, w.Hk, w.Hv, w.S, w.Dk, w.Dv, single_pass=True) == 0
+    assert gdn.prefill_workspace_bytes(4, 16, 32, 4096, 128, 128) == 0  # one pass
+    x = workloads.make_inputs(w, device=DEV)
+    ref_out, ref_st = _run(x)
+    ws = torch.full((need,), 0xAB, dtype=torch.uint8, device=DEV)  # stale contents must not matter
+    for _ in range(2):  # twice in a row with the same workspace
+        out, st = gdn.prefill(x["q"], x["k"], x["v"], x["g_log"], x["beta"], x["scale"], None, workspace=ws)
+        torch.cuda.synchronize()
+        assert torch.equal(out, ref_out) and torch.equal(st, ref_st)
+    small = ws[: need - 16]
+    out = torch.full_like(ref_out, float("nan"))
+    with pytest.raises(gdn.GdnError) as e:
+        gdn.prefill(x["q"], x["k"], x["v"], x["g_log"], x["beta"], x["scale"], None, out, workspace=small)
+    assert e.value.code == gdn.GDN_ERR_WORKSPACE
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all(), "a refused call launched work"
