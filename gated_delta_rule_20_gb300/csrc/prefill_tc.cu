@@ -798,7 +798,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         // Off the serial path: -W of each chunk, the output product, the output tile and its
         // store, and the input loads.  Thread ht reads TMEM lanes 32 (warp % 4) + ...
         const int ht = tid - kPrep - kChain;
-        int last_load = -1;  // chunks are loaded in order; this is the last one (thread ht == 0 loads)
+        // chunks are loaded in order: the first stages by thread 0, every reload by thread 32 (so
+        // that the reload does not wait behind thread 0's output product and store); the last
+        // load this thread issued
+        int last_load = -1;
         // v of the run (a map run of a split reads the zero tile for every chunk)
         const bool zero_v = kSplit && runs.run[ri].zero_v;
         const CUtensorMap* tv_run = zero_v ? &tm_v0 : &tm_v;
@@ -846,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!fail) fail = !mbar_wait_or_abort(&bars->c3, p & 1, abort_flag);
                 if (!fail) fail = !mbar_wait_or_abort(&bars->c2, p & 1, abort_flag);
                 if (named_bar_any(BAR_HELP, kHelp, fail)) break;
-                if (ht == 0 && p + kStages < n_chunks) {
+                if (ht == 32 && p + kStages < n_chunks) {
                     // reload the stage with chunk p + kStages and prefetch the chunk after into L2
                     const int t = tb + (p + kStages) * kC;
                     load_chunk(sm + sp * STAGE_BYTES, &bars->full[sp], &tm_q, &tm_k, tv_run, t, bhk, vt_of(t), vh);
@@ -893,9 +896,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         if (ht == 0) {  // drain what we issued (bounded; a completed phase returns at once)
             if (issued3 >= 0) (void)mbar_wait(&bars->c3, issued3 & 1);
-            for (int k = last_load - kStages + 1; k <= last_load; ++k)  // the last load of each stage
-                if (k >= 0) (void)mbar_wait(&bars->full[k % kStages], (k / kStages) & 1);
             tma_store_wait_all0();
+        }
+        // the last load of each stage: by ht 32 if it reloaded any stage, else the initial loads of ht 0
+        if ((ht == 32 && last_load >= 0) || (ht == 0 && n_chunks <= kStages)) {
+            for (int k = last_load - kStages + 1; k <= last_load; ++k)
+                if (k >= 0) (void)mbar_wait(&bars->full[k % kStages], (k / kStages) & 1);
         }
     }
 
