@@ -823,10 +823,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
         int issued3 = -1;  // last chunk whose output product was committed
-        // Iteration c: the output of chunk c - 1 (its product, the tile, the store, the stage
-        // reload), then -W of chunk c.  Chunk c - 1's Delta^T is waited for before chunk c's -W
-        // is announced, so the chain has taken the previous announcement and w_ready never
-        // runs two phases ahead.
+        // Iteration c: the output of chunk c - 1 (its product, the tile, the stage reload), then -W
+        // of chunk c, then the tile's store (issued after -W is announced, so that -W reaches the
+        // chain earlier).  Chunk c - 1's Delta^T is waited for before chunk c's -W is announced,
+        // so the chain has taken the previous announcement and w_ready never runs two phases
+        // ahead.
         for (int c = 0; c <= n_chunks; ++c) {
             bool fail = false;
             if (c >= 1) {
@@ -865,11 +866,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 mbar_arrive(&bars->dfree[dbp]);  // the U/W product may reuse R_D[dbp]
                 fence_proxy_async_smem();
                 named_bar_sync(BAR_HELP, kHelp);
-                if (ht == 0 && (!kSplit || runs.run[ri].write_out)) {
-                    tma_store_3d(&tm_o, sm + OFF_OUT, 0, tb + p * kC, bh);
-                    tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, tb + p * kC, bh);
-                    tma_store_commit();
-                }
             }
             if (c < n_chunks) {
                 const int s = c % kStages, db = c & 1;
@@ -892,6 +888,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 if (named_bar_any(BAR_HELP, kHelp, fail)) break;
                 mbar_arrive(&bars->w_ready);
+            }
+            // ---- the output tile of chunk c - 1 goes out once -W of chunk c is announced
+            if (c >= 1 && ht == 0 && (!kSplit || runs.run[ri].write_out)) {
+                tma_store_3d(&tm_o, sm + OFF_OUT, 0, tb + (c - 1) * kC, bh);
+                tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, tb + (c - 1) * kC, bh);
+                tma_store_commit();
             }
         }
         if (ht == 0) {  // drain what we issued (bounded; a completed phase returns at once)
