@@ -155,6 +155,22 @@ __device__ __forceinline__ void scale_row_sw128(uint8_t* tile, int row, float s)
     }
 }
 
+// The same for the four 16-byte chunks of half `hf` (physical positions 4 hf .. 4 hf + 3).
+__device__ __forceinline__ void scale_half_row_sw128(uint8_t* tile, int row, int hf, float s) {
+    const Bf16Scale sc = make_bf16_scale(s);
+    uint4* p = reinterpret_cast<uint4*>(tile + row * 128);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int q = 4 * hf + ((i + row) & 3);
+        uint4 w = p[q];
+        w.x = scale_bf16x2(w.x, sc);
+        w.y = scale_bf16x2(w.y, sc);
+        w.z = scale_bf16x2(w.z, sc);
+        w.w = scale_bf16x2(w.w, sc);
+        p[q] = w;
+    }
+}
+
 // Transposing store of one warp's 32 TMEM lanes x 64 fp32 columns, times `mul`, as bf16
 // into a pair of K-major [64 rows][64] boxes with the 128-byte swizzle (`box_stride` bytes
 // apart): lane l0 + i, column j goes to row j, element (l0 + i) % 64 of box (l0 + i) / 64.
@@ -313,7 +329,10 @@ __device__ int g_test_stall = 0;
 
 // kSplit = false: one run over whole sequences (runs.run[0], t0 = 0, len = S), the
 // instantiation a plain prefill launches; its code is that of a kernel without run tables.
-template <bool kSplit>
+// kQSplit: Q' is scaled by all eight prep warps, half a row each (warps 0..3 after their
+// diagonal block) instead of by warps 4..7 alone; measured faster when the grid runs in
+// several waves of CTAs and slower in one wave, so the host picks it by grid size.
+template <bool kSplit, bool kQSplit = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
@@ -511,7 +530,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
             // ---- warps 0..3: diagonal blocks of T;  warps 4..7: Q' = diag(gamma) Q in place, and
             //      warps 4, 5 the next chunk's decays (another slot) and the inputs of the one after
-            if (warp < 4) {
+            if (kQSplit) {
+                // row (pt % 128) % 64 of the Q box (pt % 128) / 64, 16-byte chunks 4 (pt / 128) .. + 3
+                const int qt = pt & 127;
+                if (warp < 4) solve_diag_block(M, warp, lane);
+                scale_half_row_sw128(st + ((qt >> 6) ? ST_Q1 : ST_Q0), qt & 63, pt >> 7, cGam[qt & 63]);
+                if (warp >= 4 && warp < 6) {
+                    if (c + 1 < n_chunks) scan_decays(c + 1, qt);
+                    fetch_decays(c + 2, qt);
+                }
+            } else if (warp < 4) {
                 solve_diag_block(M, warp, lane);
             } else {
                 const int qt = pt - 128;  // 0..127: row qt % 64 of the Q box qt / 64
@@ -1092,6 +1120,8 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
         if (!configured[dev]) {
             if (cudaFuncSetAttribute(gdn_prefill_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SMEM_ALLOC) != cudaSuccess ||
+                cudaFuncSetAttribute(gdn_prefill_tc_kernel<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)SMEM_ALLOC) != cudaSuccess ||
                 cudaFuncSetAttribute(gdn_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SMEM_ALLOC) != cudaSuccess ||
                 cudaFuncSetAttribute(prefill_combine_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -1106,7 +1136,10 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     const int heads = p.B * p.Hv;
     CUtensorMap tv0 = tv;  // the zero v tile of a split's map runs (unused by one-pass launches)
     auto launch = [&](const PrefillRuns& runs, int n_runs) {
-        if (n_runs == 1 && runs.run[0].t0 == 0 && runs.run[0].len == p.S)
+        if (n_runs == 1 && runs.run[0].t0 == 0 && runs.run[0].len == p.S && heads > sm_count[dev])
+            gdn_prefill_tc_kernel<false, true><<<heads, kThreads, SMEM_ALLOC, stream>>>(
+                tq, tk, tv, to, tv0, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+        else if (n_runs == 1 && runs.run[0].t0 == 0 && runs.run[0].len == p.S)
             gdn_prefill_tc_kernel<false><<<heads, kThreads, SMEM_ALLOC, stream>>>(
                 tq, tk, tv, to, tv0, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
         else
