@@ -22,7 +22,7 @@
 // tokens on N:
 //     R_G    = [Q; K] K^T       (lanes 0..63: Q K^T rows, 64..127: K K^T rows)
 //     R_D[b] = [V^T (T diag beta)^T | K^T (T diag beta gamma)^T]  -> [U^T | W^T]  (prep)
-//     R_D[b] += S0^T [-W; Q']^T  (one N = 128 product; the chain has zeroed the
+//     R_D[b] += S0^T [-W; Q']^T  (one N = 128 product; the helpers have zeroed the
 //                                 right half after reading W^T) -> [Delta^T | S0^T Q'^T]
 //     R_D[b] right half += Delta^T P^T                          -> O^T / scale
 //     R_S   += (Delta^T diag(exp(G_C - G))) K                   -> state increment, S^T layout
@@ -34,12 +34,17 @@
 //       issues the next chunk's Gram product.  Warp w reads TMEM lanes
 //       32 (w % 4) .. + 31 and, for 64-column products, columns 32 (w / 4) .. + 31.
 //   chain warps (8-11) -- the serial part, thread i on TMEM lane i: the U/W
-//       product, Delta, the state carry (fp32 S^T in TMEM, scaled by gamma_C when
-//       its bf16 copy is taken and incremented by the tensor core).
-//   helper warps (12-15) -- off the serial path: -W over V, the output product
-//       O^T += Delta^T P^T, the output tile and its TMA store, and the input
+//       product (U from thread 0, W from thread 32), Delta, the state carry
+//       (fp32 S^T in TMEM, scaled by gamma_C when its bf16 copy is taken and
+//       incremented by the tensor core).
+//   helper warps (12-15) -- off the serial path, per chunk: the output product
+//       O^T += Delta^T P^T of the previous chunk and its output tile, then -W
+//       over V of this chunk, then the previous tile's TMA store; and the input
 //       loads: a chunk's stage is reloaded with chunk c + 3 once its last
-//       product has read it, and chunk c + 4 is prefetched into L2.
+//       product has read it, and chunk c + 4 is prefetched into L2 (thread 32).
+//
+// Every run of MMAs is issued from one base shared-memory descriptor plus
+// constant offsets, which keeps each issue near its minimum cost.
 //
 // Triangular solve: (I + A)^-1 for the 64x64 strictly lower A, blocked in
 // 16x16: diagonal blocks by forward substitution in fp32, off-diagonal blocks
