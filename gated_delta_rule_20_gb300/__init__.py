@@ -22,12 +22,13 @@ from ._binding import (EXPORTED, GDN_BF16, GDN_ERR_ALIGN, GDN_ERR_CUDA, GDN_ERR_
                        GDN_ERR_TIMEOUT, GDN_ERR_UNSUPPORTED, GDN_ERR_WORKSPACE, GDN_F32, GDN_FORCE_FFMA, GDN_OK, GDN_SINGLE_PASS,
                        GDN_ZERO_INITIAL_STATE, LIB_PATH, GdnBlockDims, GdnConvDims, GdnDims, GdnError, conv1d_decode,
                        conv1d_prefill, decode_block, decode_block_noalloc, decode_block_workspace_bytes, decode_gated, decode_step,
-                       device_status, kernels_per_call, lib, make_dims, prefill, prefill_gated, prefill_segments,
+                       device_status, kernels_per_call, lib, make_dims, prefill, prefill_gated, prefill_segment_starts,
+                       prefill_segments,
                        prefill_workspace_bytes,
                        rmsnorm_gated,
                        status_string)
 
-__all__ = ["prefill", "prefill_segments", "decode_step", "conv1d_prefill", "conv1d_decode", "decode_gated", "decode_block",
+__all__ = ["prefill", "prefill_segments", "prefill_segment_starts", "decode_step", "conv1d_prefill", "conv1d_decode", "decode_gated", "decode_block",
            "decode_block_noalloc", "decode_block_workspace_bytes", "prefill_workspace_bytes", "rmsnorm_gated", "prefill_gated", "GdnBlockDims", "GdnConvDims",
            "device_status",
            "kernels_per_call", "lib", "make_dims", "status_string", "GdnDims", "GdnError", "EXPORTED", "LIB_PATH", "GDN_OK", "GDN_ERR_NULL", "GDN_ERR_DIMS",

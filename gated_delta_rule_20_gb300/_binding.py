@@ -35,7 +35,7 @@ EXPORTED = ("gdn_prefill", "gdn_decode_step", "gdn_prefill_workspace_bytes", "gd
             "gdn_device_status", "gdn_kernels_per_call", "gdn_conv1d_prefill", "gdn_conv1d_decode",
             "gdn_decode_gated", "gdn_decode_block_workspace_bytes", "gdn_decode_block", "gdn_rmsnorm_gated",
             "gdn_prefill_gated", "gdn_prefill_segments", "gdn_decode_block_noalloc",
-            "gdn_set_wait_limit_ns", "gdn_test_stall_prefill", "gdn_prefill_ws")
+            "gdn_set_wait_limit_ns", "gdn_test_stall_prefill", "gdn_prefill_ws", "gdn_prefill_segment_starts")
 
 
 class GdnDims(ctypes.Structure):
@@ -94,6 +94,9 @@ def lib() -> ctypes.CDLL:
         L.gdn_kernels_per_call.argtypes = []
         L.gdn_prefill_segments.restype = ctypes.c_int32
         L.gdn_prefill_segments.argtypes = [ctypes.POINTER(GdnDims), ctypes.c_int32]
+        L.gdn_prefill_segment_starts.restype = ctypes.c_int32
+        L.gdn_prefill_segment_starts.argtypes = [ctypes.POINTER(GdnDims), ctypes.c_int32,
+                                                 ctypes.POINTER(ctypes.c_int64), ctypes.c_int32]
         L.gdn_decode_gated.restype = ctypes.c_int
         L.gdn_decode_gated.argtypes = [vp, vp, vp, vp, fp, fp, fp, ctypes.c_float, fp, vp, ctypes.POINTER(GdnDims),
                                        vp]
@@ -312,6 +315,19 @@ def prefill_segments(B, Hk, Hv, S, Dk=128, Dv=128, dtype=GDN_BF16, sm_count=None
     flags = (GDN_FORCE_FFMA if force_ffma else 0) | (GDN_SINGLE_PASS if single_pass else 0)
     d = make_dims(B, Hk, Hv, S, Dk, Dv, dtype, flags)
     return int(lib().gdn_prefill_segments(ctypes.byref(d), int(sm_count)))
+
+
+def prefill_segment_starts(B, Hk, Hv, S, Dk=128, Dv=128, dtype=GDN_BF16, sm_count=None, *, single_pass=False,
+                           force_ffma=False) -> list:
+    """``gdn_prefill_segment_starts``: the first token of every segment of gdn_prefill's split,
+    then S (``[0, S]`` for one pass); ``[]`` for invalid dims."""
+    if sm_count is None:
+        sm_count = _torch().cuda.get_device_properties(_torch().cuda.current_device()).multi_processor_count
+    flags = (GDN_FORCE_FFMA if force_ffma else 0) | (GDN_SINGLE_PASS if single_pass else 0)
+    d = make_dims(B, Hk, Hv, S, Dk, Dv, dtype, flags)
+    buf = (ctypes.c_int64 * 17)()
+    P = int(lib().gdn_prefill_segment_starts(ctypes.byref(d), int(sm_count), buf, 17))
+    return [int(buf[j]) for j in range(P + 1)] if P > 0 else []
 
 
 def _conv_call(name, a, weight, b, c, dims, stream):

@@ -132,7 +132,7 @@ gdn_status gdn_decode_step(const void* q, const void* k, const void* v, const fl
     return gdn::launch_decode(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? GDN_OK : GDN_ERR_CUDA;
 }
 
-int32_t gdn_prefill_segments(const gdn_dims* d, int32_t sm_count) {
+int32_t gdn_prefill_segment_starts(const gdn_dims* d, int32_t sm_count, int64_t* starts, int32_t capacity) {
     if (!d || sm_count < 1) return 0;
     if ((d->dtype != GDN_F32 && d->dtype != GDN_BF16) || (d->flags & ~gdn::kKnownFlags)) return 0;
     if (d->B < 0 || d->Hk < 1 || d->Hv < 1 || d->S < 0 || d->Dk < 1 || d->Dv < 1 || d->Dk > 128 || d->Dv > 128 ||
@@ -147,8 +147,16 @@ int32_t gdn_prefill_segments(const gdn_dims* d, int32_t sm_count) {
     p.Dv = (int)d->Dv;
     p.bf16 = d->dtype == GDN_BF16;
     p.single_pass = (d->flags & GDN_SINGLE_PASS) != 0;
-    if ((d->flags & GDN_FORCE_FFMA) || !gdn::prefill_tc_supported(p)) return 1;
-    return gdn::prefill_tc_segments(p, sm_count);
+    if ((d->flags & GDN_FORCE_FFMA) || !gdn::prefill_tc_supported(p)) p.single_pass = true;
+    long long buf[17];
+    const int P = gdn::prefill_tc_segment_starts(p, sm_count, buf, 17);
+    if (starts && capacity >= P + 1)
+        for (int j = 0; j <= P; ++j) starts[j] = P > 1 ? buf[j] : (j == 0 ? 0 : d->S);
+    return P;
+}
+
+int32_t gdn_prefill_segments(const gdn_dims* d, int32_t sm_count) {
+    return gdn_prefill_segment_starts(d, sm_count, nullptr, 0);
 }
 
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims) {

@@ -43,8 +43,11 @@ bool prefill_tc_supported(const Problem& p);
 // Segments the tensor-core prefill splits each sequence into on a device with `sms` SMs
 // (1: one pass).
 int prefill_tc_segments(const Problem& p, int sms);
-// Device scratch of launch_prefill_tc on a device with `sms` SMs: the segment states and maps
-// of a split (0 for one pass).
+// The same, and with capacity >= P + 1 the segments' first tokens in starts[0 .. P - 1] and
+// S in starts[P].
+int prefill_tc_segment_starts(const Problem& p, int sms, long long* starts, int capacity);
+// Device scratch of launch_prefill_tc on a device with `sms` SMs: the segment states, maps
+// and the identity-start runs' outputs of a split (0 for one pass).
 size_t prefill_tc_workspace_bytes(const Problem& p, int sms);
 // workspace == nullptr: a split takes stream-ordered scratch itself (and runs one pass if it
 // cannot be had); otherwise the caller's buffer of workspace_bytes >=

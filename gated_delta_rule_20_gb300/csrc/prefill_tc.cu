@@ -59,7 +59,11 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <utility>
+#include <vector>
 
 #include "gdn_internal.h"
 #include "sm100_ptx.cuh"
@@ -311,15 +315,16 @@ __device__ __forceinline__ void prefetch_chunk_l2(const CUtensorMap* tq, const C
 // A launch processes up to kMaxRuns runs over the same heads: run r covers tokens
 // t0 .. t0 + len - 1 of every (batch, value head) sequence, CTA blockIdx.x = r * heads + head.
 // A plain prefill is one run over the whole sequence; a split one (host side, below) uses
-// runs over segments, some of them state-only runs from a zero start or from the identity
-// with v = 0.
+// runs over segments, some of them from a zero start or from the identity with v = 0.
 struct PrefillRun {
     const float* state_in;  // initial states, head h at state_in + h * in_stride; nullptr: zero
     float* state_out;       // final states [heads, Dk, Dv]; may equal state_in
     long long in_stride;    // Dk * Dv, or 0 (one start state for every head)
     int t0, len;            // len >= 1; every run but a sequence's last covers whole chunks
-    int write_out;          // 0: the outputs are not stored (a run that only yields a state)
+    int write_out;          // 0: outputs not stored; 1: to out; 2: to the second output map, at
+                            // token t - out_shift
     int zero_v;             // 1: v = 0 (every chunk's v tile read from the 64-token zero map)
+    int out_shift;
 };
 constexpr int kMaxRuns = 32;
 struct PrefillRuns {
@@ -341,7 +346,7 @@ template <bool kSplit, bool kQSplit = false>
 __global__ void __launch_bounds__(kThreads, 1)
     gdn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
-                          const __grid_constant__ CUtensorMap tm_v0,
+                          const __grid_constant__ CUtensorMap tm_v0, const __grid_constant__ CUtensorMap tm_c,
                           const float* __restrict__ g_log, const float* __restrict__ beta,
                           const __grid_constant__ PrefillRuns runs, float scale, int Hk, int Hv, int S,
                           int32_t* __restrict__ status) {
@@ -844,7 +849,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_prefetch_desc(&tm_q);
             tma_prefetch_desc(&tm_k);
             tma_prefetch_desc(tv_run);
-            tma_prefetch_desc(&tm_o);
+            tma_prefetch_desc(kSplit && runs.run[ri].write_out == 2 ? &tm_c : &tm_o);
             for (int c = 0; c < kStages && c < n_chunks; ++c) {
                 const int t = tb + c * kC;
                 load_chunk(sm + c * STAGE_BYTES, &bars->full[c], &tm_q, &tm_k, tv_run, t, bhk, vt_of(t), vh);
@@ -924,8 +929,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             // ---- the output tile of chunk c - 1 goes out once -W of chunk c is announced
             if (c >= 1 && ht == 0 && (!kSplit || runs.run[ri].write_out)) {
-                tma_store_3d(&tm_o, sm + OFF_OUT, 0, tb + (c - 1) * kC, bh);
-                tma_store_3d(&tm_o, sm + OFF_OUT + 8192, 64, tb + (c - 1) * kC, bh);
+                // to out, or (a split's identity-start runs) to the second map
+                const bool to_c = kSplit && runs.run[ri].write_out == 2;
+                const CUtensorMap* tmo = to_c ? &tm_c : &tm_o;
+                const int t = tb - (to_c ? runs.run[ri].out_shift : 0) + (c - 1) * kC;
+                tma_store_3d(tmo, sm + OFF_OUT, 0, t, bh);
+                tma_store_3d(tmo, sm + OFF_OUT + 8192, 64, t, bh);
                 tma_store_commit();
             }
         }
@@ -979,14 +988,22 @@ bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_
 }
 
 // ---------------------------------------------------------------- split sequences
-// Start states of the later segments of a split prefill: for j = 1 .. n_maps,
-//     S_{j+1} = M_j S_j + X_j.
-// The chunk recurrence is affine in its start state (S_end = M S0 + X): X_j is segment j's
-// final state from a zero start, M_j its final state from S0 = I with v = 0.  Each state
-// column evolves on its own: blockIdx.x = head, blockIdx.y = a slice of kCols columns, and
-// the slices exchange nothing.  256 threads, thread t: row t / 2, kCols / 2 columns; plain
-// fp32 FMAs.  M_{j+1} and this slice of X_{j+1} reach shared memory by cp.async while step j
-// computes, so each step pays one copy latency at most.
+// A split prefill runs segment 0 of every sequence from the real start state and, for each
+// later segment j = 1 .. P - 1, two runs at once: one from a zero start (its outputs out_0
+// go to out, its end state is X_j) and one from S0 = I with v = 0 (its end state is M_j, its
+// outputs C go to a scratch tensor).  The chunk recurrence is affine in its start state, so
+// segment j's end state is M_j S_j + X_j and its output at token t is out_0[t] + C[t] S_j:
+// with v = 0 and S0 = I the run computes scale (q'_t - P_t W_t) M_t, the linear part of
+// the output in the start state (M_t the map from the segment's start to chunk t's).  Then
+// the combine step chains S_{j+1} = M_j S_j + X_j into every start state (the last one is
+// the final state), and the correction adds C[t] S_j to the outputs of segments 1 .. P - 1.
+
+// Combine: for j = 1 .. n_maps, S_{j+1} = M_j S_j + X_j; S_{j+1} goes to slot j of Sst, the
+// last one (the final state) to `last`.  Each state column evolves on its own: blockIdx.x =
+// head, blockIdx.y = a slice of kCols columns, and the slices exchange nothing.  256
+// threads, thread t: row t / 2, kCols / 2 columns; plain fp32 FMAs.  M_{j+1} and this slice
+// of X_{j+1} reach shared memory by cp.async while step j computes, so each step pays one
+// copy latency at most.
 constexpr int kCombStride = kD + 4;  // padded rows of M, 16-byte aligned: the 16 rows a warp reads
                                      // fall on 8 distinct 16-byte bank groups
 template <int kCols>
@@ -996,7 +1013,8 @@ constexpr size_t comb_smem() {  // raw M_j; M_j with padded rows; the S_j slice;
 
 template <int kCols>
 __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ X, const float* __restrict__ Mg,
-                                                              float* __restrict__ Sst, int heads, int n_maps) {
+                                                              float* __restrict__ Sst, float* __restrict__ last,
+                                                              int heads, int n_maps) {
     extern __shared__ __align__(16) float csm[];
     float* rawM = csm;                  // [128][128] M_j as copied
     float* sM = rawM + kD * kD;         // [128][132] M_j
@@ -1048,7 +1066,7 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
             }
         }
         __syncthreads();  // every thread has read the S_j slice
-        float* Sn = Sst + ((size_t)j * heads + h) * hs;  // S_{j+1}
+        float* Sn = (j == n_maps ? last + (size_t)h * hs : Sst + ((size_t)j * heads + h) * hs);  // S_{j+1}
 #pragma unroll
         for (int e = 0; e < kPer; ++e) {
             const float v = acc[e] + sX[r * kCols + c0 + e];
@@ -1058,24 +1076,318 @@ __global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __res
     }
 }
 
+// Correction: out[t] += C[t] S_j over the tokens of segments 1 .. P - 1, in tiles of 128
+// tokens (segments 1 .. P - 2 hold whole tiles; the last one ends at S).  One tcgen05
+// product per tile, D[128 tokens][Dv] = C_tile[128][Dk] S_j[Dk][Dv]: A = the C tile
+// (K-major, two 64-column halves of 128 rows with the 128-byte swizzle, loaded by TMA),
+// B = S_j^T in bf16 (K-major: row dv, dk along the row; built in shared memory from the
+// fp32 state).  The fp32 result plus the out_0 tile (loaded by TMA with it) is rounded to
+// bf16 in place and stored over out_0 by TMA.  A persistent grid: CTA c takes a contiguous
+// range of the tiles, ordered by segment, then head, then token, so it rebuilds B only
+// where its range crosses into another (segment, head).
+// Roles (192 threads): warp 0 lane 0 loads through kCorrStages stages, warp 1 lane 0 issues
+// the products into two TMEM accumulators, warps 2..5 (one TMEM lane quadrant each, thread
+// = token row) build B and write the tiles back.
+constexpr int kCorrStages = 3;
+constexpr int kCorrThreads = 192;
+constexpr uint32_t CORR_HALF = 16384;          // [128 rows][64 bf16], 128-byte swizzle
+constexpr uint32_t CORR_TILE = 2 * CORR_HALF;  // one 128 x 128 bf16 operand
+constexpr uint32_t CORR_OFF_B = 0;
+constexpr uint32_t CORR_OFF_ST = CORR_TILE;    // stage s: the C tile, then the out tile
+constexpr uint32_t CORR_STAGE = 2 * CORR_TILE;
+constexpr uint32_t CORR_OFF_BAR = CORR_OFF_ST + kCorrStages * CORR_STAGE;
+constexpr uint32_t CORR_SMEM = CORR_OFF_BAR + 256 + 1024;
+static_assert(CORR_SMEM <= 232448, "shared memory budget");
+constexpr uint32_t IDESC_CORR = make_idesc_bf16(128, 128, 0, 0);
+constexpr uint32_t BAR_CORR_EPI = 1;  // named barrier: the 4 write-back warps
+
+struct CorrBars {
+    uint64_t full[kCorrStages];
+    uint64_t empty[kCorrStages];
+    uint64_t done[2];     // accumulator a's product has completed
+    uint64_t afree[2];    // accumulator a has been read (128 arrivals)
+    uint64_t b_ready;     // B holds the next (segment, head)'s state (128 arrivals per build)
+    uint32_t tmem_base;
+    int abort;
+};
+static_assert(sizeof(CorrBars) <= 256, "CorrBars");
+
+struct CorrArgs {
+    const float* states;  // S_1 .. S_{P-1}: pair p = (j - 1) * heads + h at states + p * Dk * Dv
+    int heads;
+    int tiles_seg;    // 128-token tiles per segment
+    int total;        // heads * (P - 1) * tiles_seg
+    int s1;           // first token of segment 1 = row 0 of the C tensor
+    int seg_tokens;   // tokens per segment 1 .. P - 2 (a multiple of 128)
+    int S;
+};
+
+__global__ void __launch_bounds__(kCorrThreads, 1)
+    prefill_correct_kernel(const __grid_constant__ CUtensorMap tm_c, const __grid_constant__ CUtensorMap tm_o,
+                           const __grid_constant__ CorrArgs args, int32_t* __restrict__ status) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t* sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sbase = smem_u32(sm);
+    CorrBars* bars = reinterpret_cast<CorrBars*>(sm + CORR_OFF_BAR);
+    volatile int* abort_flag = &bars->abort;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int g0 = (int)((long long)blockIdx.x * args.total / gridDim.x);
+    const int n = (int)((long long)(blockIdx.x + 1) * args.total / gridDim.x) - g0;
+    auto pair_of = [&](int i) { return (g0 + i) / args.tiles_seg; };
+    auto token_of = [&](int i) {  // first token of this CTA's tile i
+        const int g = g0 + i, p = g / args.tiles_seg;
+        return args.s1 + (p / args.heads) * args.seg_tokens + (g - p * args.tiles_seg) * 128;
+    };
+
+    if (tid == 0) {
+        for (int s = 0; s < kCorrStages; ++s) {
+            mbar_init(&bars->full[s], 1);
+            mbar_init(&bars->empty[s], 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(&bars->done[a], 1);
+            mbar_init(&bars->afree[a], 128);
+        }
+        mbar_init(&bars->b_ready, 128);
+        bars->abort = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) {
+        tmem_alloc(&bars->tmem_base, 256);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = bars->tmem_base;
+
+    if (warp == 0) {
+        if (lane == 0) {  // TMA loads: the C tile and the out_0 tile, 64-token halves inside the sequence
+            tma_prefetch_desc(&tm_c);
+            tma_prefetch_desc(&tm_o);
+            int loaded = 0;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % kCorrStages;
+                if (i >= kCorrStages &&
+                    !mbar_wait_or_abort(&bars->empty[s], (i / kCorrStages - 1) & 1, abort_flag))
+                    break;
+                const int t0 = token_of(i), h = pair_of(i) % args.heads;
+                const int halves = t0 + 64 < args.S ? 2 : 1;
+                uint8_t* st = sm + CORR_OFF_ST + s * CORR_STAGE;
+                mbar_arrive_expect_tx(&bars->full[s], (uint32_t)halves * 4 * 8192);
+                for (int kh = 0; kh < 2; ++kh)
+                    for (int th = 0; th < halves; ++th) {
+                        tma_load_3d(st + kh * CORR_HALF + th * 8192, &tm_c, &bars->full[s], kh * 64,
+                                    t0 - args.s1 + th * 64, h);
+                        tma_load_3d(st + CORR_TILE + kh * CORR_HALF + th * 8192, &tm_o, &bars->full[s], kh * 64,
+                                    t0 + th * 64, h);
+                    }
+                loaded = i + 1;
+            }
+            // drain: every issued load has landed before the CTA can exit (bounded)
+            for (int i = (loaded > kCorrStages ? loaded - kCorrStages : 0); i < loaded; ++i)
+                (void)mbar_wait(&bars->full[i % kCorrStages], (i / kCorrStages) & 1);
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {  // the products, accumulator i % 2
+            const uint64_t db = make_sdesc(sbase + CORR_OFF_B, 16, 1024);
+            int cur = -1, builds = 0, issued = 0;
+            for (int i = 0; i < n; ++i) {
+                const int s = i % kCorrStages, a = i & 1, p = pair_of(i);
+                if (p != cur) {  // B of the tile's pair
+                    if (!mbar_wait_or_abort(&bars->b_ready, builds & 1, abort_flag)) break;
+                    ++builds;
+                    cur = p;
+                }
+                if (!mbar_wait_or_abort(&bars->full[s], (i / kCorrStages) & 1, abort_flag)) break;
+                if (i >= 2 && !mbar_wait_or_abort(&bars->afree[a], ((i >> 1) - 1) & 1, abort_flag)) break;
+                tc_fence_after();
+                const uint64_t da = make_sdesc(sbase + CORR_OFF_ST + s * CORR_STAGE, 16, 1024);
+#pragma unroll
+                for (int kh = 0; kh < 2; ++kh)
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16(tmem + a * 128, sdesc_add(da, kh * CORR_HALF + kk * 32),
+                                 sdesc_add(db, kh * CORR_HALF + kk * 32), IDESC_CORR, (kh | kk) != 0);
+                mma_commit(&bars->done[a]);
+                issued = i + 1;
+            }
+            // drain: the last commit covers every product issued (bounded)
+            if (issued > 0) (void)mbar_wait(&bars->done[(issued - 1) & 1], ((issued - 1) >> 1) & 1);
+        }
+    } else {  // warps 2..5
+        const int et = tid - 64;
+        const int quad = warp & 3;
+        const int r = quad * 32 + lane;  // token row of the tile = TMEM lane
+        const uint32_t trow = tmem + ((uint32_t)(quad * 32) << 16);
+        int cur = -1;
+        for (int i = 0; i < n; ++i) {
+            const int s = i % kCorrStages, a = i & 1, p = pair_of(i);
+            if (p != cur) {
+                // B = S_j^T in bf16 for pair p.  Every product of the previous pair has completed
+                // (this thread waited for the previous tile's).  Thread (w, l): dv columns
+                // 4l .. 4l + 3 and dk rows 8 kc .. 8 kc + 7 for kc = w, w + 4, w + 8, w + 12.
+                const float* Sg = args.states + (size_t)p * kD * kD;
+                const int w = et >> 5, l = et & 31;
+#pragma unroll 1
+                for (int u = 0; u < 4; ++u) {
+                    const int kc = w + 4 * u;
+                    float4 v[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e)
+                        v[e] = __ldg(reinterpret_cast<const float4*>(Sg + (size_t)(kc * 8 + e) * kD) + l);
+                    uint8_t* bh = sm + CORR_OFF_B + (kc >> 3) * CORR_HALF;
+                    const uint32_t byte = (kc & 7) * 16;
+                    *reinterpret_cast<uint4*>(bh + sw128_offset(4 * l + 0, byte)) =
+                        make_uint4(pack_bf16x2(v[0].x, v[1].x), pack_bf16x2(v[2].x, v[3].x),
+                                   pack_bf16x2(v[4].x, v[5].x), pack_bf16x2(v[6].x, v[7].x));
+                    *reinterpret_cast<uint4*>(bh + sw128_offset(4 * l + 1, byte)) =
+                        make_uint4(pack_bf16x2(v[0].y, v[1].y), pack_bf16x2(v[2].y, v[3].y),
+                                   pack_bf16x2(v[4].y, v[5].y), pack_bf16x2(v[6].y, v[7].y));
+                    *reinterpret_cast<uint4*>(bh + sw128_offset(4 * l + 2, byte)) =
+                        make_uint4(pack_bf16x2(v[0].z, v[1].z), pack_bf16x2(v[2].z, v[3].z),
+                                   pack_bf16x2(v[4].z, v[5].z), pack_bf16x2(v[6].z, v[7].z));
+                    *reinterpret_cast<uint4*>(bh + sw128_offset(4 * l + 3, byte)) =
+                        make_uint4(pack_bf16x2(v[0].w, v[1].w), pack_bf16x2(v[2].w, v[3].w),
+                                   pack_bf16x2(v[4].w, v[5].w), pack_bf16x2(v[6].w, v[7].w));
+                }
+                fence_proxy_async_smem();
+                mbar_arrive(&bars->b_ready);
+                cur = p;
+            }
+            // the product, and the out_0 tile (its load is waited for here too, so that this
+            // thread observes it)
+            bool fail = !mbar_wait_or_abort(&bars->done[a], (i >> 1) & 1, abort_flag);
+            if (!fail) fail = !mbar_wait_or_abort(&bars->full[s], (i / kCorrStages) & 1, abort_flag);
+            if (named_bar_any(BAR_CORR_EPI, 128, fail)) break;
+            tc_fence_after();
+            uint8_t* ot = sm + CORR_OFF_ST + s * CORR_STAGE + CORR_TILE;
+#pragma unroll 1
+            for (int cb = 0; cb < 4; ++cb) {  // dv columns 32 cb .. 32 cb + 31
+                float x[32];
+                tmem_ld32(trow + a * 128 + cb * 32, x);
+                tmem_wait_ld();
+                uint8_t* half = ot + (cb >> 1) * CORR_HALF;
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint4* q = reinterpret_cast<uint4*>(half + sw128_offset(r, (cb & 1) * 64 + ch * 16));
+                    uint4 o = *q;
+                    const float* xc = x + 8 * ch;
+                    o.x = pack_bf16x2(bf16lo_to_f32(o.x) + xc[0], bf16hi_to_f32(o.x) + xc[1]);
+                    o.y = pack_bf16x2(bf16lo_to_f32(o.y) + xc[2], bf16hi_to_f32(o.y) + xc[3]);
+                    o.z = pack_bf16x2(bf16lo_to_f32(o.z) + xc[4], bf16hi_to_f32(o.z) + xc[5]);
+                    o.w = pack_bf16x2(bf16lo_to_f32(o.w) + xc[6], bf16hi_to_f32(o.w) + xc[7]);
+                    *q = o;
+                }
+            }
+            tc_fence_before();
+            mbar_arrive(&bars->afree[a]);
+            fence_proxy_async_smem();
+            named_bar_sync(BAR_CORR_EPI, 128);
+            if (et == 0) {
+                const int t0 = token_of(i), h = p % args.heads;
+                const int halves = t0 + 64 < args.S ? 2 : 1;
+                for (int kh = 0; kh < 2; ++kh)
+                    for (int th = 0; th < halves; ++th)
+                        tma_store_3d(&tm_o, ot + kh * CORR_HALF + th * 8192, kh * 64, t0 + th * 64, h);
+                tma_store_commit();
+                if (i >= 1) {  // the previous tile's store has read its stage: the stage may be reloaded
+                    tma_store_wait_read1();
+                    mbar_arrive(&bars->empty[(i - 1) % kCorrStages]);
+                }
+            }
+        }
+        if (et == 0) tma_store_wait_all0();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && bars->abort) atomicExch(status, (int32_t)GDN_ERR_TIMEOUT);
+    if (warp == 1) tmem_dealloc(tmem, 256);
+}
+
 // A Dk x Dv identity (one CTA per row).
 __global__ void identity_kernel(float* I) { I[blockIdx.x * kD + threadIdx.x] = blockIdx.x == threadIdx.x ? 1.f : 0.f; }
 
-// Segments for a prefill of `heads` sequences of n_chunks chunks on `sms` SMs (1: no split).
-// A split into P segments runs in two waves of about n_chunks / P chunks: first segment 0
-// from the real start state and, for each middle segment, one run from a zero start and one
-// from the identity with v = 0 (heads * (2P - 3) CTAs, one per SM); then segments 1 .. P - 1 from the
-// start states the combine kernel derives.  Worth it from P = 3, with segments of at least
-// 8 chunks; 2P - 3 runs must fit one launch.
-int split_segments(int heads, int n_chunks, int sms) {
-    if (heads * 3 > sms) return 1;
-    int P = (sms - heads) / (2 * heads) + 2;
-    P = P < (kMaxRuns + 3) / 2 ? P : (kMaxRuns + 3) / 2;
-    P = P < n_chunks / 8 ? P : n_chunks / 8;
-    if (P < 3) return 1;
-    const int L = (n_chunks + P - 1) / P;
-    P = (n_chunks + L - 1) / L;
-    return P >= 3 ? P : 1;
+// ---------------------------------------------------------------- split plan
+// Segment 0 has a chunks, segments 1 .. P - 1 have x chunks each (x even: whole correction
+// tiles; the last segment ends at S).  P = 1: one pass.
+struct SplitPlan {
+    int P = 1, a = 0, x = 0;
+};
+constexpr int kMaxSegments = (kMaxRuns + 1) / 2;
+
+// Finish time, in chunk periods, of one launch of `heads` runs of a chunks followed by
+// 2 heads (P - 1) runs of x chunks, one CTA per SM, each CTA starting (in launch order) on
+// the SM that frees first.
+long split_makespan(int heads, int sms, int P, int a, int x) {
+    std::vector<std::pair<long, long>> groups{{0, sms}};  // (time an SM frees up, SMs)
+    long end = 0;
+    auto assign = [&](long runs, long dur) {
+        while (runs > 0) {
+            size_t gi = 0;
+            for (size_t g = 1; g < groups.size(); ++g)
+                if (groups[g].first < groups[gi].first) gi = g;
+            const long m = runs < groups[gi].second ? runs : groups[gi].second;
+            const long t = groups[gi].first + dur;
+            runs -= m;
+            end = t > end ? t : end;
+            if ((groups[gi].second -= m) == 0) groups.erase(groups.begin() + (long)gi);
+            bool merged = false;
+            for (auto& g : groups)
+                if (g.first == t) {
+                    g.second += m;
+                    merged = true;
+                }
+            if (!merged) groups.push_back({t, m});
+        }
+    };
+    assign(heads, a);
+    assign(2L * heads * (P - 1), x);
+    return end;
+}
+
+// Predicted time of a split, in us: the runs launch at kPeriodUs a chunk, the combine step
+// (P - 1 steps in sequence) and the correction, which streams C, out_0 and out (768 bytes a
+// token) at kCorrBytesPerUs.  Measured on a GB300 (152 SMs, one CTA per SM).
+constexpr double kPeriodUs = 3.0;
+constexpr double kCombUs = 8.0, kCombStepUs = 5.0;
+constexpr double kCorrUs = 6.0, kCorrBytesPerUs = 5.5e6;
+
+SplitPlan plan_split_uncached(int heads, int S, int sms) {
+    const int n = (S + kC - 1) / kC;
+    SplitPlan best;
+    double best_us = 0.9 * n * kPeriodUs;  // a split must save a tenth of one pass
+    for (int P = 2; P <= kMaxSegments; ++P)
+        for (int x = 2; (long)(P - 1) * x < n; x += 2) {
+            const int a = n - (P - 1) * x;
+            const double us = (double)split_makespan(heads, sms, P, a, x) * kPeriodUs + kCombUs +
+                              (P - 1) * kCombStepUs + kCorrUs +
+                              (double)heads * (S - a * kC) * 768.0 / kCorrBytesPerUs;
+            if (us < best_us) {
+                best_us = us;
+                best = {P, a, x};
+            }
+        }
+    return best;
+}
+
+// The plan for (heads, S, SMs), computed once per shape.
+SplitPlan plan_split(int heads, int S, int sms) {
+    if (heads < 1 || S < 1 || sms < 1) return {};
+    static std::mutex mu;
+    static std::map<std::tuple<int, int, int>, SplitPlan> cache;
+    const auto key = std::make_tuple(heads, S, sms);
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        auto it = cache.find(key);
+        if (it != cache.end()) return it->second;
+    }
+    const SplitPlan plan = plan_split_uncached(heads, S, sms);
+    std::lock_guard<std::mutex> lock(mu);
+    if (cache.size() > 4096) cache.clear();
+    cache[key] = plan;
+    return plan;
 }
 
 }  // namespace
@@ -1092,19 +1404,36 @@ cudaError_t set_prefill_tc_test_stall(int on) {
     return cudaMemcpyToSymbol(g_test_stall, &v, sizeof(v));
 }
 
-int prefill_tc_segments(const Problem& p, int sms) {
-    if (p.single_pass || p.B == 0 || p.S == 0) return 1;
-    return split_segments(p.B * p.Hv, (p.S + kC - 1) / kC, sms);
+namespace {
+SplitPlan plan_for(const Problem& p, int sms) {
+    if (p.single_pass || p.B == 0 || p.S == 0 || !prefill_tc_supported(p)) return {};
+    return plan_split(p.B * p.Hv, p.S, sms);
+}
+}  // namespace
+
+int prefill_tc_segments(const Problem& p, int sms) { return plan_for(p, sms).P; }
+
+int prefill_tc_segment_starts(const Problem& p, int sms, long long* starts, int capacity) {
+    const SplitPlan plan = plan_for(p, sms);
+    if (starts && capacity >= plan.P + 1) {
+        starts[0] = 0;
+        for (int j = 1; j < plan.P; ++j) starts[j] = (long long)(plan.a + (j - 1) * plan.x) * kC;
+        starts[plan.P] = p.S;
+    }
+    return plan.P;
 }
 
-// Split scratch: S_1 .. S_{P-1}, X_1 .. X_{P-2}, M_1 .. M_{P-2} (one state per head each), one
-// identity and one zero v tile [64 tokens][128] bf16.
+// Split scratch: S_1 .. S_{P-1}, X_1 .. X_{P-1}, M_1 .. M_{P-1} (one fp32 state per head each),
+// one identity, one zero v tile [64 tokens][128] bf16, and C [heads][S - s1][128] bf16 (the
+// identity-start runs' outputs over segments 1 .. P - 1, s1 the first token of segment 1).
 constexpr size_t kZeroTile = (size_t)kC * kD * 2;
 size_t prefill_tc_workspace_bytes(const Problem& p, int sms) {
-    const int P = prefill_tc_segments(p, sms);
-    if (P <= 1) return 0;
-    const size_t hs = (size_t)p.B * p.Hv * kD * kD;
-    return ((size_t)(3 * P - 5) * hs + (size_t)kD * kD) * sizeof(float) + kZeroTile;
+    const SplitPlan plan = plan_for(p, sms);
+    if (plan.P <= 1) return 0;
+    const size_t heads = (size_t)p.B * p.Hv;
+    const size_t hs = heads * kD * kD;
+    return ((size_t)(3 * (plan.P - 1)) * hs + (size_t)kD * kD) * sizeof(float) + kZeroTile +
+           heads * (size_t)(p.S - plan.a * kC) * kD * 2;
 }
 
 gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_t stream, void* workspace,
@@ -1133,29 +1462,31 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
                                      (int)comb_smem<16>()) != cudaSuccess ||
                 cudaFuncSetAttribute(prefill_combine_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)comb_smem<32>()) != cudaSuccess ||
+                cudaFuncSetAttribute(prefill_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)CORR_SMEM) != cudaSuccess ||
                 cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
                 return GDN_ERR_CUDA;
             configured[dev] = true;
         }
     }
     const int heads = p.B * p.Hv;
-    CUtensorMap tv0 = tv;  // the zero v tile of a split's map runs (unused by one-pass launches)
+    CUtensorMap tv0 = tv, tc = to;  // the zero v tile and the C tensor of a split (unused by one pass)
     auto launch = [&](const PrefillRuns& runs, int n_runs) {
         if (n_runs == 1 && runs.run[0].t0 == 0 && runs.run[0].len == p.S && heads > sm_count[dev])
             gdn_prefill_tc_kernel<false, true><<<heads, kThreads, SMEM_ALLOC, stream>>>(
-                tq, tk, tv, to, tv0, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+                tq, tk, tv, to, tv0, tc, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
         else if (n_runs == 1 && runs.run[0].t0 == 0 && runs.run[0].len == p.S)
             gdn_prefill_tc_kernel<false><<<heads, kThreads, SMEM_ALLOC, stream>>>(
-                tq, tk, tv, to, tv0, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+                tq, tk, tv, to, tv0, tc, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
         else
             gdn_prefill_tc_kernel<true><<<heads * n_runs, kThreads, SMEM_ALLOC, stream>>>(
-                tq, tk, tv, to, tv0, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
+                tq, tk, tv, to, tv0, tc, p.g_log, p.beta, runs, p.scale, p.Hk, p.Hv, p.S, status_word);
         return cudaGetLastError() == cudaSuccess;
     };
     PrefillRuns runs{};
     runs.heads = heads;
-    const int n_chunks = (p.S + kC - 1) / kC;
-    const int P = prefill_tc_segments(p, sm_count[dev]);
+    const SplitPlan plan = plan_for(p, sm_count[dev]);
+    const int P = plan.P;
     const size_t hs = (size_t)heads * kD * kD;  // floats in one state per head
     const long long one = (long long)kD * kD;  // floats in one head's state
     // the split's scratch: the caller's workspace, else stream-ordered memory
@@ -1174,39 +1505,49 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
         }
     }
     if (!ws) {  // one run over the whole sequence
-        runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S, 1, 0};
+        runs.run[0] = {p.zero_init ? nullptr : p.state, p.state, one, 0, p.S, 1, 0, 0};
         return launch(runs, 1) ? GDN_OK : GDN_ERR_CUDA;
     }
     float* Sst = static_cast<float*>(ws);
     float* X = Sst + (size_t)(P - 1) * hs;
-    float* M = X + (size_t)(P - 2) * hs;
-    float* I = M + (size_t)(P - 2) * hs;
-    void* Z = I + one;
-    const int L = (n_chunks + P - 1) / P * kC;  // tokens per segment; the last one takes the rest
+    float* M = X + (size_t)(P - 1) * hs;
+    float* I = M + (size_t)(P - 1) * hs;
+    uint8_t* Z = reinterpret_cast<uint8_t*>(I + one);
+    void* C = Z + kZeroTile;
+    const int s1 = plan.a * kC, xs = plan.x * kC;  // first token of segment 1; tokens per later segment
     identity_kernel<<<kD, kD, 0, stream>>>(I);
     bool ok = cudaGetLastError() == cudaSuccess && cudaMemsetAsync(Z, 0, kZeroTile, stream) == cudaSuccess &&
-              encode_bf16_3d(&tv0, Z, 1, kC, 64, true);
-    runs.run[0] = {p.zero_init ? nullptr : p.state, Sst, one, 0, L, 1, 0};
-    for (int j = 1; j <= P - 2; ++j) {  // the map runs store no outputs
-        runs.run[2 * j - 1] = {nullptr, X + (size_t)(j - 1) * hs, one, j * L, L, 0, 0};
-        // from S0 = I with v = 0: the end state is the segment's linear map M_j itself
-        runs.run[2 * j] = {I, M + (size_t)(j - 1) * hs, 0, j * L, L, 0, 1};
+              encode_bf16_3d(&tv0, Z, 1, kC, 64, true) && encode_bf16_3d(&tc, C, heads, p.S - s1, 64, true);
+    runs.run[0] = {p.zero_init ? nullptr : p.state, Sst, one, 0, s1, 1, 0, 0};
+    for (int j = 1; j < P; ++j) {
+        const int t0 = s1 + (j - 1) * xs, len = j < P - 1 ? xs : p.S - t0;
+        runs.run[2 * j - 1] = {nullptr, X + (size_t)(j - 1) * hs, one, t0, len, 1, 0, 0};
+        // from S0 = I with v = 0: the end state is the segment's linear map M_j, the outputs C
+        runs.run[2 * j] = {I, M + (size_t)(j - 1) * hs, 0, t0, len, 2, 1, s1};
     }
-    ok = ok && launch(runs, 2 * P - 3);
+    ok = ok && launch(runs, 2 * P - 1);
     if (ok) {
         // one CTA per SM (about 210 KB of shared memory): 16-column slices while they fit one wave
         if (heads * (kD / 16) <= sm_count[dev])
-            prefill_combine_kernel<16><<<dim3(heads, kD / 16), 256, comb_smem<16>(), stream>>>(X, M, Sst, heads, P - 2);
+            prefill_combine_kernel<16><<<dim3(heads, kD / 16), 256, comb_smem<16>(), stream>>>(X, M, Sst, p.state,
+                                                                                                heads, P - 1);
         else
-            prefill_combine_kernel<32><<<dim3(heads, kD / 32), 256, comb_smem<32>(), stream>>>(X, M, Sst, heads, P - 2);
+            prefill_combine_kernel<32><<<dim3(heads, kD / 32), 256, comb_smem<32>(), stream>>>(X, M, Sst, p.state,
+                                                                                                heads, P - 1);
         ok = cudaGetLastError() == cudaSuccess;
     }
     if (ok) {
-        for (int j = 1; j <= P - 1; ++j) {
-            float* Sj = Sst + (size_t)(j - 1) * hs;
-            runs.run[j - 1] = {Sj, j == P - 1 ? p.state : Sj, one, j * L, j == P - 1 ? p.S - j * L : L, 1, 0};
-        }
-        ok = launch(runs, P - 1);
+        CorrArgs ca{};
+        ca.states = Sst;
+        ca.heads = heads;
+        ca.tiles_seg = plan.x / 2;
+        ca.total = heads * (P - 1) * ca.tiles_seg;
+        ca.s1 = s1;
+        ca.seg_tokens = xs;
+        ca.S = p.S;
+        const int grid = ca.total < sm_count[dev] ? ca.total : sm_count[dev];
+        prefill_correct_kernel<<<grid, kCorrThreads, CORR_SMEM, stream>>>(tc, to, ca, status_word);
+        ok = cudaGetLastError() == cudaSuccess;
     }
     if (own) ok = cudaFreeAsync(ws, stream) == cudaSuccess && ok;
     return ok ? GDN_OK : GDN_ERR_CUDA;

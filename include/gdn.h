@@ -105,22 +105,25 @@ typedef struct {
  * tcgen05 tensor-core kernel; every other supported shape and fp32 compute run
  * on the FFMA kernel.
  *
- * Few long sequences (on the tensor-core path, at most a third as many
- * sequences B * Hv as SMs, and at least 24 chunks of 64 tokens each) are split
- * into P >= 3 segments unless GDN_SINGLE_PASS is set.  The recurrence is affine
- * in its start state, so a middle segment's end state is X + M S0, with X its
- * end state from a zero start and M its end state from S0 = I with v = 0.  Four
- * launches: an identity matrix; segment 0 from the real start state together
- * with both runs of every middle segment; a combine step that chains the maps
- * into every segment's start state (fp32); segments 1 .. P - 1 from those start
- * states.  Every output element is written once, by the run that owns its
- * token (the zero- and identity-start runs store none), so out is written as
- * in one pass.  The scratch (3P - 5 states per sequence and one identity) is
- * allocated with
- * cudaMallocAsync on `stream` and freed there; if that allocation fails, the
- * call runs one pass instead.  The results agree with the one-pass form to
- * within rounding (the same error against an fp64 reference, from strong decay
- * to none), not bit for bit.
+ * Few long sequences (on the tensor-core path) are split into P >= 2 segments
+ * unless GDN_SINGLE_PASS is set, when a host-side model of the launch (one CTA
+ * per SM, CTAs dispatched in order) predicts that it saves at least a tenth of
+ * one pass; gdn_prefill_segment_starts reports the split.  The recurrence is
+ * affine in its start state: a later segment's end state is M S0 + X and its
+ * output at token t is out_0[t] + C[t] S0, with X and out_0 its end state and
+ * outputs from a zero start and M and C (C[t]: 1 x Dk per token) its end state
+ * and outputs from S0 = I with v = 0.  Five launches: an identity matrix; one
+ * launch of segment 0 from the real start state and both runs of every later
+ * segment (out_0 is written to out, C to the scratch); a combine step that
+ * chains the maps into every segment's start state and the final state
+ * (fp32); a correction that adds C[t] S0 to the later segments' outputs
+ * (tcgen05, S0 rounded to bf16; the sum rounded once to bf16).  The scratch
+ * (gdn_prefill_workspace_bytes: 3 (P - 1) states per sequence, one identity,
+ * and C for every token after segment 0) is allocated with cudaMallocAsync on
+ * `stream` and freed there; if that allocation fails, the call runs one pass
+ * instead.  The results agree with the one-pass form to within rounding (the
+ * same error against an fp64 reference, from strong decay to none), not bit for
+ * bit; segment 0's outputs are those of one pass.
  */
 gdn_status gdn_prefill(const void* q, const void* k, const void* v,
                        const float* g_log, const float* beta, float scale,
@@ -333,8 +336,8 @@ gdn_status gdn_prefill_gated(const void* q, const void* k, const void* v, const 
                              const gdn_dims* dims, gdn_stream_t stream);
 
 /* Device scratch a prefill with these dims needs on the current device: the
- * segment states and maps of a split (see gdn_prefill; the split depends on
- * the device's SM count), 0 when the call runs one pass.  0 as well for
+ * segment states, maps and identity-start outputs of a split (see gdn_prefill;
+ * the split depends on the device's SM count), 0 when the call runs one pass.  0 as well for
  * invalid dims or when no CUDA device can be queried.  Host only. */
 size_t gdn_prefill_workspace_bytes(const gdn_dims* dims);
 
@@ -358,8 +361,15 @@ gdn_status gdn_prefill_ws(const void* q, const void* k, const void* v,
 /* Segments gdn_prefill splits each sequence into for these dims on a device
  * with sm_count SMs (see gdn_prefill): 1 for one pass (every shape off the
  * tensor-core path, GDN_FORCE_FFMA, GDN_SINGLE_PASS, B == 0 or S == 0),
- * otherwise 3 .. 17.  0 for invalid dims or sm_count < 1.  Host only. */
+ * otherwise 2 .. 16.  0 for invalid dims or sm_count < 1.  Host only. */
 int32_t gdn_prefill_segments(const gdn_dims* dims, int32_t sm_count);
+
+/* gdn_prefill_segments, and where the segments start: with starts != NULL and
+ * capacity >= P + 1 (P the return value), starts[j] is the first token of
+ * segment j (starts[0] = 0) and starts[P] = S.  Segment 0 may be longer than
+ * the others; segments 1 .. P - 2 have the same multiple of 128 tokens and the
+ * last one ends at S.  No counterpart on the pages.  Host only. */
+int32_t gdn_prefill_segment_starts(const gdn_dims* dims, int32_t sm_count, int64_t* starts, int32_t capacity);
 
 /* Static, NUL-terminated description of a status code. */
 const char* gdn_status_string(gdn_status s);

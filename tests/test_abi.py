@@ -111,18 +111,16 @@ def test_empty_batch_is_a_no_op(L):
 
 
 def test_prefill_segments():
-    """The split rule of gdn_prefill (host only): at most a third as many sequences as SMs,
-    segments of 8 chunks or more, at most 17; one pass off the tensor-core path or when
-    asked for; 0 for invalid dims."""
+    """The split rule of gdn_prefill (host only): few long sequences split into 2 .. 16
+    segments where the launch model predicts a saving; one pass off the tensor-core path or
+    when asked for; 0 for invalid dims."""
     seg = gdn.prefill_segments
-    assert seg(1, 16, 32, 32768, sm_count=152) == 3       # the long workload: 32 sequences
+    assert seg(1, 16, 32, 32768, sm_count=152) == 6       # the long workload: 32 sequences
     assert seg(4, 16, 32, 4096, sm_count=152) == 1        # 128 sequences: one pass
-    assert seg(1, 1, 2, 32768, sm_count=152) == 17        # capped by the run table
-    assert seg(1, 1, 1, 1536, sm_count=152) == 3          # 24 chunks: three of 8
-    assert seg(1, 1, 1, 1472, sm_count=152) == 1          # 23 chunks
-    assert seg(2, 5, 25, 1536, sm_count=152) == 3         # 50 sequences, 150 CTAs in the first launch
-    assert seg(2, 5, 25, 1536, sm_count=148) == 1         # 3 x 50 > 148
-    assert seg(1, 1, 8, 16384, sm_count=152) == 11
+    assert seg(16, 8, 32, 2048, sm_count=152) == 1        # 512 sequences: one pass
+    assert seg(1, 1, 2, 32768, sm_count=152) == 16        # capped by the run table
+    assert seg(2, 5, 25, 1536, sm_count=152) == 2         # 50 sequences: 150 CTAs in one wave
+    assert seg(1, 1, 1, 256, sm_count=152) == 1           # 4 chunks: too short to pay
     assert seg(1, 1, 2, 32768, dtype=gdn.GDN_F32, sm_count=152) == 1
     assert seg(1, 1, 2, 32768, Dk=64, Dv=64, sm_count=152) == 1
     assert seg(1, 1, 2, 32768, sm_count=152, single_pass=True) == 1
@@ -133,6 +131,27 @@ def test_prefill_segments():
     assert seg(1, 1, 2, 4096, sm_count=0) == 0
     L = gdn.lib()
     assert L.gdn_prefill_segments(None, 152) == 0
+
+
+def test_prefill_segment_starts():
+    """Segment bounds of the split (host only): segment 0 from token 0, segments 1 .. P - 2
+    of one multiple of 128 tokens, the last one ending at S (ragged S included); one pass
+    gives [0, S]; the count agrees with gdn_prefill_segments on every shape."""
+    st = gdn.prefill_segment_starts
+    assert st(1, 16, 32, 32768, sm_count=152) == [0, 12288, 16384, 20480, 24576, 28672, 32768]
+    assert st(4, 16, 32, 4096, sm_count=152) == [0, 4096]
+    assert st(1, 1, 2, 4096, sm_count=152, single_pass=True) == [0, 4096]
+    assert st(1, 2, 3, 4096, sm_count=152) == []
+    for B, Hk, Hv, S in [(1, 1, 2, 2000), (1, 1, 1, 4608), (2, 2, 8, 3072), (1, 1, 2, 3000), (1, 2, 4, 2500),
+                         (2, 5, 25, 1536), (2, 4, 32, 8192), (1, 1, 8, 16385), (1, 1, 64, 32768), (1, 1, 2, 32767)]:
+        b = st(B, Hk, Hv, S, sm_count=152)
+        assert len(b) - 1 == gdn.prefill_segments(B, Hk, Hv, S, sm_count=152) >= 2
+        assert b[0] == 0 and b[-1] == S and all(x < y for x, y in zip(b, b[1:]))
+        assert b[1] % 64 == 0
+        mids = {y - x for x, y in zip(b[1:-2], b[2:-1])}
+        assert len(mids) <= 1 and all(m % 128 == 0 for m in mids)
+        if len(b) > 3:
+            assert 0 < S - b[-2] <= b[2] - b[1]   # the last segment: at most one middle segment
 
 
 def test_prefill_flags_known(L):

@@ -1,10 +1,11 @@
-"""The split prefill (gdn.h, gdn_prefill): on the tensor-core path, few sequences (B * Hv at
-most a third of the SM count) of at least 24 chunks are split into segments, whose start
-states come from each middle segment's end states from a zero and an identity start (the
-chunk recurrence is affine in its start state).  Checked here: parity with the fp64 oracle,
-agreement with the one-pass form (GDN_SINGLE_PASS), a ragged last segment, zero and supplied
-start states, GQA, weak decay (so that every segment's state map matters), strong decay,
-determinism, NaN-prefilled outputs with guard bands, and replay in a CUDA graph."""
+"""The split prefill (gdn.h, gdn_prefill): on the tensor-core path, few long sequences are
+split into segments; every later segment runs from a zero start and from the identity with
+v = 0 (the chunk recurrence is affine in its start state), a combine step chains the maps
+into the start states, and a correction adds the start state's part to the later segments'
+outputs.  Checked here: parity with the fp64 oracle, agreement with the one-pass form
+(GDN_SINGLE_PASS), a ragged last segment, zero and supplied start states, GQA, weak decay
+(so that every segment's state map matters), strong decay, determinism, NaN-prefilled
+outputs with guard bands, the caller's workspace, and replay in a CUDA graph."""
 import pytest
 import torch
 
@@ -29,6 +30,11 @@ def segments(w):
     return gdn.prefill_segments(w.B, w.Hk, w.Hv, w.S)
 
 
+def starts(w):
+    """The first token of every segment gdn_prefill picks for workload w on this GPU, then S."""
+    return gdn.prefill_segment_starts(w.B, w.Hk, w.Hv, w.S)
+
+
 # name, B, Hk, Hv, S, state std, log-decay range, beta std, seed; each case is compared with
 # the oracle over the whole output and final-state tensors
 CASES = [
@@ -39,9 +45,10 @@ CASES = [
     ("b1_hk2_hv4_s2500_strong_decay", 1, 2, 4, 2500, 0.05, (-2.0, -0.001), 2.0, 105),
     # almost no decay: the state persists through every segment, so the maps carry it
     ("b1_hv2_s4096_almost_no_decay", 1, 1, 2, 4096, 0.05, (-1e-4, -1e-6), 1.0, 107),
-    # at the thresholds: 50 sequences (a third of 152 SMs: 150 CTAs in the first launch) and
-    # 24 chunks exactly (3 segments of 8 chunks)
-    ("b2_hk5_hv25_s1536_threshold", 2, 5, 25, 1536, 0.02, (-0.5, -0.005), 1.0, 106),
+    # 50 sequences (two segments: 150 CTAs in one wave) and 24 chunks
+    ("b2_hk5_hv25_s1536_two_segments", 2, 5, 25, 1536, 0.02, (-0.5, -0.005), 1.0, 106),
+    # 64 sequences: the runs take two waves of CTAs
+    ("b2_hk4_hv32_s8192_two_waves", 2, 4, 32, 8192, 0.02, (-0.5, -0.005), 1.0, 108),
 ]
 
 
@@ -62,7 +69,7 @@ def _run(x, single_pass=False):
 @pytest.mark.parametrize("case", CASES, ids=[c[0] for c in CASES])
 def test_split_prefill_matches_oracle(case):
     w, x = _inputs(case)
-    if segments(w) < 3:  # every case splits on a 152-SM GB300
+    if segments(w) < 2:  # every case splits on a 152-SM GB300
         pytest.skip("not split on this GPU")
     out, st = _run(x)
     ro, rs = oracle_for(x)
@@ -77,9 +84,8 @@ def test_split_prefill_agrees_with_one_pass(case):
     assert rel_l2(to64(o1), to64(o2)) < 1e-2
     assert rel_l2(to64(s1), to64(s2)) < 1e-2
     # segment 0 runs from the real start state in both forms, on the same kernel and tokens
-    n = (w.S + 63) // 64
-    P = segments(w)
-    L = 64 * ((n + P - 1) // P)
+    L = starts(w)[1]
+    assert 0 < L < w.S
     assert torch.equal(o1[:, :, :L], o2[:, :, :L])
 
 
@@ -147,8 +153,9 @@ def test_caller_workspace_matches_own_scratch():
     w = workloads.LONG_PREFILL.with_(S=8192, seed=31)
     assert segments(w) > 1
     need = gdn.prefill_workspace_bytes(w.B, w.Hk, w.Hv, w.S, w.Dk, w.Dv)
-    P = segments(w)
-    assert need == ((3 * P - 5) * w.B * w.Hv * 128 * 128 + 128 * 128) * 4 + 64 * 128 * 2
+    P, s1, heads = segments(w), starts(w)[1], w.B * w.Hv
+    # 3 (P - 1) states per sequence, one identity, the zero v tile, C after segment 0 (bf16)
+    assert need == (3 * (P - 1) * heads * 128 * 128 + 128 * 128) * 4 + 64 * 128 * 2 + heads * (w.S - s1) * 128 * 2
     assert gdn.prefill_workspace_bytes(w.B, w.Hk, w.Hv, w.S, w.Dk, w.Dv, single_pass=True) == 0
     assert gdn.prefill_workspace_bytes(4, 16, 32, 4096, 128, 128) == 0  # one pass
     x = workloads.make_inputs(w, device=DEV)
