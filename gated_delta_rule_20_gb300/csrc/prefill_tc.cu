@@ -485,6 +485,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (pt >= 128 && pt < 192) {
             fetch_decays(1, pt - 128);
         }
+        // chunk 0's decays are read by every prep thread (masks, Q'): the chunk's input load
+        // alone does not order them after the scan (it may land first, from L2)
+        named_bar_sync(BAR_PREP, kPrep);
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c % kStages;  // input stage
             uint8_t* st = sm + s * STAGE_BYTES;
@@ -1000,78 +1003,114 @@ bool encode_bf16_3d(CUtensorMap* map, const void* ptr, int heads, int S, uint32_
 
 // Combine: for j = 1 .. n_maps, S_{j+1} = M_j S_j + X_j; S_{j+1} goes to slot j of Sst, the
 // last one (the final state) to `last`.  Each state column evolves on its own: blockIdx.x =
-// head, blockIdx.y = a slice of kCols columns, and the slices exchange nothing.  256
-// threads, thread t: row t / 2, kCols / 2 columns; plain fp32 FMAs.  M_{j+1} and this slice
-// of X_{j+1} reach shared memory by cp.async while step j computes, so each step pays one
-// copy latency at most.
-constexpr int kCombStride = kD + 4;  // padded rows of M, 16-byte aligned: the 16 rows a warp reads
-                                     // fall on 8 distinct 16-byte bank groups
-template <int kCols>
-constexpr size_t comb_smem() {  // raw M_j; M_j with padded rows; the S_j slice; the X_j slice (two buffers)
-    return (size_t)(kD * kD + kD * kCombStride + 3 * kD * kCols) * sizeof(float);
-}
+// head, blockIdx.y = a slice of 32 columns, and the slices exchange nothing.  Plain fp32
+// FMAs, blocked in registers: thread t takes the k quarter t / 64 and, with g = t % 64,
+// rows g / 4 + 16 i and columns 8 (g % 4) + c (i, c = 0..7), so that each value read from
+// shared memory feeds 8 FMAs; the four quarters' partial sums meet in shared memory.  M_j
+// lands by cp.async in one of two buffers; M_{j+1} and this slice of X_{j+1} are copied into
+// the other one while step j computes, and the spent M_j buffer holds the partial sums.
+// Row strides (floats): M 132 (the 8 rows a warp reads at once fall on distinct 16-byte
+// bank groups), the S_j slice 36, the partial sums 36.
+constexpr int kCombCols = 32;
+constexpr int kCombThreads = 256;
+constexpr int kCombMS = kD + 4;
+constexpr int kCombSS = kCombCols + 4;
+// M_j (two buffers); the S_j slice; the X_j slice (two buffers)
+constexpr size_t kCombSmem = (size_t)(2 * kD * kCombMS + kD * kCombSS + 2 * kD * kCombCols) * sizeof(float);
+static_assert(3 * kD * kCombSS <= kD * kCombMS, "the partial sums fit a spent M buffer");
 
-template <int kCols>
-__global__ void __launch_bounds__(256) prefill_combine_kernel(const float* __restrict__ X, const float* __restrict__ Mg,
-                                                              float* __restrict__ Sst, float* __restrict__ last,
-                                                              int heads, int n_maps) {
+__global__ void __launch_bounds__(kCombThreads, 1)
+    prefill_combine_kernel(const float* __restrict__ X, const float* __restrict__ Mg, float* __restrict__ Sst,
+                           float* __restrict__ last, int heads, int n_maps) {
     extern __shared__ __align__(16) float csm[];
-    float* rawM = csm;                  // [128][128] M_j as copied
-    float* sM = rawM + kD * kD;         // [128][132] M_j
-    float* sS = sM + kD * kCombStride;  // [128][kCols] this slice of S_j
-    float* sXb = sS + kD * kCols;       // [2][128][kCols] this slice of X_j, buffer j % 2
-    const int h = blockIdx.x, col0 = blockIdx.y * kCols, t = threadIdx.x;
+    float* sMb = csm;                    // [2][128][132] M_j, buffer j % 2
+    float* sS = sMb + 2 * kD * kCombMS;  // [128][36] this slice of S_j
+    float* sXb = sS + kD * kCombSS;      // [2][128][32] this slice of X_j, buffer j % 2
+    const int h = blockIdx.x, col0 = blockIdx.y * kCombCols, t = threadIdx.x;
     const size_t hs = (size_t)kD * kD;
-    constexpr int kVecs = kCols / 4;    // 16-byte pieces of a slice row
+    constexpr int kVecs = kCombCols / 4;  // 16-byte pieces of a slice row
     auto copy_maps = [&](int j) {
         const float* Mj = Mg + ((size_t)(j - 1) * heads + h) * hs;
         const float* Xj = X + ((size_t)(j - 1) * heads + h) * hs;
-        float* sXj = sXb + (j & 1) * kD * kCols;
-        for (int i = t; i < kD * kD / 4; i += 256) cp_async_16(rawM + 4 * i, Mj + 4 * i);
-        for (int i = t; i < kD * kVecs; i += 256)  // only the slice's columns of X_j
+        float* sMj = sMb + (j & 1) * kD * kCombMS;
+        float* sXj = sXb + (j & 1) * kD * kCombCols;
+        for (int i = t; i < kD * kD / 4; i += kCombThreads)
+            cp_async_16(sMj + (4 * i / kD) * kCombMS + 4 * i % kD, Mj + 4 * i);
+        for (int i = t; i < kD * kVecs; i += kCombThreads)  // only the slice's columns of X_j
             cp_async_16(sXj + 4 * i, Xj + (size_t)(i / kVecs) * kD + col0 + 4 * (i % kVecs));
         cp_async_commit();
     };
     copy_maps(1);
     const float* S1 = Sst + (size_t)h * hs;
-    for (int i = t; i < kD * kCols; i += 256) sS[i] = S1[(size_t)(i / kCols) * kD + col0 + i % kCols];
-    constexpr int kPer = kCols / 2;
-    const int r = t >> 1, c0 = (t & 1) * kPer;
+    for (int i = t; i < kD * kCombCols; i += kCombThreads)
+        sS[(i / kCombCols) * kCombSS + i % kCombCols] = S1[(size_t)(i / kCombCols) * kD + col0 + i % kCombCols];
+    const int kq = t >> 6, g = t & 63;
+    const int r0 = g >> 2, c0 = (g & 3) * 8;  // rows r0 + 16 i, columns c0 .. c0 + 7
     for (int j = 1; j <= n_maps; ++j) {
-        const float* sX = sXb + (j & 1) * kD * kCols;
+        float* sM = sMb + (j & 1) * kD * kCombMS;
+        const float* sX = sXb + (j & 1) * kD * kCombCols;
         cp_async_wait_all();
-        __syncthreads();  // M_j, the X_j slice and the S_j slice are in shared memory
-        for (int i = t; i < kD * kD / 4; i += 256)
-            *reinterpret_cast<float4*>(sM + (4 * i / kD) * kCombStride + 4 * i % kD) =
-                reinterpret_cast<const float4*>(rawM)[i];
-        __syncthreads();  // M_j is built; the raw buffer is free (the X_j slice stays in its buffer)
+        __syncthreads();  // M_j, the X_j slice and the S_j slice are in shared memory; step j - 1's
+                          // buffers are free
         if (j < n_maps) copy_maps(j + 1);
-        float acc[kPer];
+        float acc[8][8];
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) acc[e] = 0.f;
-        for (int k = 0; k < kD; k += 4) {  // four k per 16-byte read of M's row
-            const float4 m4 = *reinterpret_cast<const float4*>(sM + r * kCombStride + k);
-            const float mk[4] = {m4.x, m4.y, m4.z, m4.w};
+        for (int i = 0; i < 8; ++i)
 #pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const float4* srow = reinterpret_cast<const float4*>(sS + (k + kk) * kCols + c0);
+            for (int c = 0; c < 8; ++c) acc[i][c] = 0.f;
+        const float* mrow = sM + r0 * kCombMS + kq * 32;
+        const float* scol = sS + kq * 32 * kCombSS + c0;
+#pragma unroll 1
+        for (int kk = 0; kk < 32; kk += 4) {
+            float4 a[8];
 #pragma unroll
-                for (int q = 0; q < kPer / 4; ++q) {
-                    const float4 v = srow[q];
-                    acc[4 * q + 0] = fmaf(mk[kk], v.x, acc[4 * q + 0]);
-                    acc[4 * q + 1] = fmaf(mk[kk], v.y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(mk[kk], v.z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(mk[kk], v.w, acc[4 * q + 3]);
+            for (int i = 0; i < 8; ++i) a[i] = *reinterpret_cast<const float4*>(mrow + i * 16 * kCombMS + kk);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 b0 = *reinterpret_cast<const float4*>(scol + (kk + u) * kCombSS);
+                const float4 b1 = *reinterpret_cast<const float4*>(scol + (kk + u) * kCombSS + 4);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const float m = u == 0 ? a[i].x : u == 1 ? a[i].y : u == 2 ? a[i].z : a[i].w;
+                    acc[i][0] = fmaf(m, b0.x, acc[i][0]);
+                    acc[i][1] = fmaf(m, b0.y, acc[i][1]);
+                    acc[i][2] = fmaf(m, b0.z, acc[i][2]);
+                    acc[i][3] = fmaf(m, b0.w, acc[i][3]);
+                    acc[i][4] = fmaf(m, b1.x, acc[i][4]);
+                    acc[i][5] = fmaf(m, b1.y, acc[i][5]);
+                    acc[i][6] = fmaf(m, b1.z, acc[i][6]);
+                    acc[i][7] = fmaf(m, b1.w, acc[i][7]);
                 }
             }
         }
-        __syncthreads();  // every thread has read the S_j slice
-        float* Sn = (j == n_maps ? last + (size_t)h * hs : Sst + ((size_t)j * heads + h) * hs);  // S_{j+1}
+        __syncthreads();  // every thread has read M_j and the S_j slice
+        float* red = sM;  // [3][128][36]: the partial sums of k quarters 1..3
+        if (kq > 0) {
 #pragma unroll
-        for (int e = 0; e < kPer; ++e) {
-            const float v = acc[e] + sX[r * kCols + c0 + e];
-            sS[r * kCols + c0 + e] = v;  // read in step j + 1 after its first barrier
-            Sn[(size_t)r * kD + col0 + c0 + e] = v;
+            for (int i = 0; i < 8; ++i) {
+                float* d = red + ((kq - 1) * kD + r0 + 16 * i) * kCombSS + c0;
+                *reinterpret_cast<float4*>(d) = make_float4(acc[i][0], acc[i][1], acc[i][2], acc[i][3]);
+                *reinterpret_cast<float4*>(d + 4) = make_float4(acc[i][4], acc[i][5], acc[i][6], acc[i][7]);
+            }
+        }
+        __syncthreads();  // the partial sums are in shared memory
+        if (kq == 0) {
+            float* Sn = (j == n_maps ? last + (size_t)h * hs : Sst + ((size_t)j * heads + h) * hs);  // S_{j+1}
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int r = r0 + 16 * i;
+                float v[8];
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    v[c] = acc[i][c] + red[r * kCombSS + c0 + c] + red[(kD + r) * kCombSS + c0 + c] +
+                           red[(2 * kD + r) * kCombSS + c0 + c] + sX[r * kCombCols + c0 + c];
+                // read in step j + 1 after its first barrier
+                *reinterpret_cast<float4*>(sS + r * kCombSS + c0) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(sS + r * kCombSS + c0 + 4) = make_float4(v[4], v[5], v[6], v[7]);
+                float* o = Sn + (size_t)r * kD + col0 + c0;
+                *reinterpret_cast<float4*>(o) = make_float4(v[0], v[1], v[2], v[3]);
+                *reinterpret_cast<float4*>(o + 4) = make_float4(v[4], v[5], v[6], v[7]);
+            }
         }
     }
 }
@@ -1317,19 +1356,19 @@ struct SplitPlan {
 };
 constexpr int kMaxSegments = (kMaxRuns + 1) / 2;
 
-// Finish time, in chunk periods, of one launch of `heads` runs of a chunks followed by
-// 2 heads (P - 1) runs of x chunks, one CTA per SM, each CTA starting (in launch order) on
-// the SM that frees first.
-long split_makespan(int heads, int sms, int P, int a, int x) {
-    std::vector<std::pair<long, long>> groups{{0, sms}};  // (time an SM frees up, SMs)
-    long end = 0;
-    auto assign = [&](long runs, long dur) {
+// Finish time, in us, of one launch of `heads` runs of duration da followed by
+// 2 heads (P - 1) runs of duration dx, one CTA per SM, each CTA starting (in launch order)
+// on the SM that frees first.
+double split_makespan(int heads, int sms, int P, double da, double dx) {
+    std::vector<std::pair<double, long>> groups{{0.0, sms}};  // (time an SM frees up, SMs)
+    double end = 0.0;
+    auto assign = [&](long runs, double dur) {
         while (runs > 0) {
             size_t gi = 0;
             for (size_t g = 1; g < groups.size(); ++g)
                 if (groups[g].first < groups[gi].first) gi = g;
             const long m = runs < groups[gi].second ? runs : groups[gi].second;
-            const long t = groups[gi].first + dur;
+            const double t = groups[gi].first + dur;
             runs -= m;
             end = t > end ? t : end;
             if ((groups[gi].second -= m) == 0) groups.erase(groups.begin() + (long)gi);
@@ -1342,33 +1381,39 @@ long split_makespan(int heads, int sms, int P, int a, int x) {
             if (!merged) groups.push_back({t, m});
         }
     };
-    assign(heads, a);
-    assign(2L * heads * (P - 1), x);
+    assign(heads, da);
+    assign(2L * heads * (P - 1), dx);
     return end;
 }
 
-// Predicted time of a split, in us: the runs launch at kPeriodUs a chunk, the combine step
-// (P - 1 steps in sequence) and the correction, which streams C, out_0 and out (768 bytes a
-// token) at kCorrBytesPerUs.  Measured on a GB300 (152 SMs, one CTA per SM).
-constexpr double kPeriodUs = 3.0;
-constexpr double kCombUs = 8.0, kCombStepUs = 5.0;
-constexpr double kCorrUs = 6.0, kCorrBytesPerUs = 5.5e6;
+// Predicted time of a split, in us, from measurements on a GB300 (152 SMs): a run takes
+// kRunUs plus kPeriodUs a chunk -- kPeriodFullUs for the later segments' runs when the
+// launch has more CTAs than SMs (they then share the GPU with every other run and were
+// measured slower) -- the combine step kCombUs plus kCombStepUs a step, and the correction
+// kCorrUs plus its bytes (C, out_0 and out: 768 a token) at kCorrBytesPerUs.  One pass:
+// kOnePeriodUs a chunk.
+constexpr double kPeriodUs = 2.95, kPeriodFullUs = 3.4, kRunUs = 4.0, kLaunchUs = 5.0;
+constexpr double kCombUs = 6.0, kCombStepUs = 3.0;
+constexpr double kCorrUs = 4.0, kCorrBytesPerUs = 6.2e6;
+constexpr double kOnePeriodUs = 2.8;
 
 SplitPlan plan_split_uncached(int heads, int S, int sms) {
     const int n = (S + kC - 1) / kC;
     SplitPlan best;
-    double best_us = 0.9 * n * kPeriodUs;  // a split must save a tenth of one pass
-    for (int P = 2; P <= kMaxSegments; ++P)
+    double best_us = 0.9 * (n * kOnePeriodUs + kLaunchUs);  // a split must save a tenth of one pass
+    for (int P = 2; P <= kMaxSegments; ++P) {
+        const double px = (long)heads * (2 * P - 1) > sms ? kPeriodFullUs : kPeriodUs;
         for (int x = 2; (long)(P - 1) * x < n; x += 2) {
             const int a = n - (P - 1) * x;
-            const double us = (double)split_makespan(heads, sms, P, a, x) * kPeriodUs + kCombUs +
-                              (P - 1) * kCombStepUs + kCorrUs +
+            const double us = split_makespan(heads, sms, P, kRunUs + a * kPeriodUs, kRunUs + x * px) + kLaunchUs +
+                              kCombUs + (P - 1) * kCombStepUs + kCorrUs +
                               (double)heads * (S - a * kC) * 768.0 / kCorrBytesPerUs;
             if (us < best_us) {
                 best_us = us;
                 best = {P, a, x};
             }
         }
+    }
     return best;
 }
 
@@ -1458,10 +1503,8 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
                                      (int)SMEM_ALLOC) != cudaSuccess ||
                 cudaFuncSetAttribute(gdn_prefill_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)SMEM_ALLOC) != cudaSuccess ||
-                cudaFuncSetAttribute(prefill_combine_kernel<16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)comb_smem<16>()) != cudaSuccess ||
-                cudaFuncSetAttribute(prefill_combine_kernel<32>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     (int)comb_smem<32>()) != cudaSuccess ||
+                cudaFuncSetAttribute(prefill_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     (int)kCombSmem) != cudaSuccess ||
                 cudaFuncSetAttribute(prefill_correct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                      (int)CORR_SMEM) != cudaSuccess ||
                 cudaDeviceGetAttribute(&sm_count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
@@ -1527,13 +1570,9 @@ gdn_status launch_prefill_tc(const Problem& p, int32_t* status_word, cudaStream_
     }
     ok = ok && launch(runs, 2 * P - 1);
     if (ok) {
-        // one CTA per SM (about 210 KB of shared memory): 16-column slices while they fit one wave
-        if (heads * (kD / 16) <= sm_count[dev])
-            prefill_combine_kernel<16><<<dim3(heads, kD / 16), 256, comb_smem<16>(), stream>>>(X, M, Sst, p.state,
-                                                                                                heads, P - 1);
-        else
-            prefill_combine_kernel<32><<<dim3(heads, kD / 32), 256, comb_smem<32>(), stream>>>(X, M, Sst, p.state,
-                                                                                                heads, P - 1);
+        // four 32-column slices per head, one CTA per SM (182 KB of shared memory)
+        prefill_combine_kernel<<<dim3(heads, kD / kCombCols), kCombThreads, kCombSmem, stream>>>(X, M, Sst, p.state,
+                                                                                             heads, P - 1);
         ok = cudaGetLastError() == cudaSuccess;
     }
     if (ok) {

@@ -219,6 +219,19 @@ def test_prefill_deterministic():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+@pytest.mark.parametrize("B,Hk,Hv", [(4, 16, 32), (16, 8, 32)], ids=["one_wave", "several_waves"])
+def test_prefill_deterministic_full_size(B, Hk, Hv):
+    """One pass at a full-size shape (one wave of CTAs, and 512 sequences in several waves),
+    repeated: bit-identical outputs and states, with the inputs of the first chunks warm in L2
+    after the first call."""
+    w = workloads.PREFILL.with_(B=B, Hk=Hk, Hv=Hv, S=2048, seed=22)
+    x = workloads.make_inputs(w, device=DEV)
+    o1, s1 = run_prefill(x)
+    for _ in range(6):
+        o2, s2 = run_prefill(x)
+        assert torch.equal(o1, o2) and torch.equal(s1, s2)
+
+
 def test_prefill_empty_sequence():
     w = small("bf16", S=0, seed=3)
     x = workloads.make_inputs(w, device=DEV)

@@ -118,6 +118,20 @@ def test_split_prefill_deterministic():
     assert torch.equal(o1, o2) and torch.equal(s1, s2)
 
 
+def test_split_prefill_deterministic_over_many_waves():
+    """A split whose runs take several waves of CTAs (32 sequences, later segments paired on
+    the same inputs), repeated: every output and state bit-identical.  Catches ordering races
+    inside a CTA that only show when a run's first input load lands early (from L2) -- such
+    a race perturbs a segment's first chunks by less than the parity tolerance."""
+    w = workloads.LONG_PREFILL.with_(S=8192, seed=31)
+    assert segments(w) > 1
+    x = workloads.make_inputs(w, device=DEV)
+    ref_out, ref_st = _run(x)
+    for _ in range(10):
+        out, st = _run(x)
+        assert torch.equal(out, ref_out) and torch.equal(st, ref_st)
+
+
 def test_split_prefill_graph_replay():
     """The split form (its stream-ordered scratch included) captured in a CUDA graph and
     replayed gives the eager result bit for bit."""
