@@ -572,9 +572,11 @@ def run_ours(args, rank, world, local_rank):
     long_prefill = {"workload": wl.name, "split": long_leg(False), "single_pass": long_leg(True),
                     "algorithmic_bytes": lbytes, "algorithmic_flops": lflops,
                     "workspace_bytes": lws_bytes,
-                    "note": "split: segment 0 and two state-only runs per middle segment, a combine step, "
-                            "then the remaining segments (2 prefill launches, an identity fill and the "
-                            "combine), scratch in a caller workspace allocated before timing; inputs larger "
+                    "segment_starts": gdn.prefill_segment_starts(wl.B, wl.Hk, wl.Hv, wl.S),
+                    "note": "split: one launch of segment 0 and, per later segment, a zero-start and an "
+                            "identity-start run (several CTA waves); a combine step; a tensor-core "
+                            "correction of the later segments' outputs (plus an identity fill and a "
+                            "memset); scratch in a caller workspace allocated before timing; inputs larger "
                             "than L2"}
     del xl, lout, lws
 

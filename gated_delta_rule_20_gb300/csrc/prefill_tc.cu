@@ -1356,64 +1356,70 @@ struct SplitPlan {
 };
 constexpr int kMaxSegments = (kMaxRuns + 1) / 2;
 
-// Finish time, in us, of one launch of `heads` runs of duration da followed by
-// 2 heads (P - 1) runs of duration dx, one CTA per SM, each CTA starting (in launch order)
-// on the SM that frees first.
-double split_makespan(int heads, int sms, int P, double da, double dx) {
+// Predicted time of a split, in us, fitted to measurements on a GB300 (152 SMs, plans of
+// 2 to 12 segments for 32 and 64 sequences of 8192 and 32768 tokens; within 3 % on the 32768
+// ones).  A run costs kRunUs plus a period per chunk: kPeriodAUs for segment 0; for the
+// later segments' runs from kPeriodLoUs up to kPeriodHiUs as the CTAs running at their start
+// go from 128 to 152 (measured: the more CTAs run, the slower each one).  Then the combine
+// (kCombStepUs a step), the correction (768 bytes a token -- C, out_0 and out -- at
+// kCorrBytesPerUs) and kFixedUs for the launches.  One pass: kOnePeriodUs a chunk.
+constexpr double kPeriodAUs = 2.95, kPeriodLoUs = 2.8, kPeriodHiUs = 3.3, kRunUs = 2.0;
+constexpr double kCombStepUs = 3.0, kCorrBytesPerUs = 7.0e6, kFixedUs = 44.5;
+constexpr double kOnePeriodUs = 2.8, kOneFixedUs = 5.0;
+
+// Finish time, in us, of one launch of `heads` runs of a chunks followed by 2 heads (P - 1)
+// runs of x chunks, one CTA per SM, each CTA starting (in launch order) on the SM that frees
+// first.
+double split_makespan(int heads, int sms, int P, int a, int x) {
     std::vector<std::pair<double, long>> groups{{0.0, sms}};  // (time an SM frees up, SMs)
     double end = 0.0;
-    auto assign = [&](long runs, double dur) {
+    auto assign = [&](long runs, int chunks, bool later) {
         while (runs > 0) {
             size_t gi = 0;
             for (size_t g = 1; g < groups.size(); ++g)
                 if (groups[g].first < groups[gi].first) gi = g;
+            const double t = groups[gi].first;
             const long m = runs < groups[gi].second ? runs : groups[gi].second;
-            const double t = groups[gi].first + dur;
+            long busy = m;  // CTAs running once these start
+            for (const auto& g : groups)
+                if (g.first > t) busy += g.second;
+            double period = kPeriodAUs;
+            if (later) {
+                const double f = (double)(busy - 128) / 24.0;
+                period = kPeriodLoUs + (kPeriodHiUs - kPeriodLoUs) * (f < 0.0 ? 0.0 : f > 1.0 ? 1.0 : f);
+            }
+            const double te = t + kRunUs + chunks * period;
             runs -= m;
-            end = t > end ? t : end;
+            end = te > end ? te : end;
             if ((groups[gi].second -= m) == 0) groups.erase(groups.begin() + (long)gi);
             bool merged = false;
             for (auto& g : groups)
-                if (g.first == t) {
+                if (g.first == te) {
                     g.second += m;
                     merged = true;
                 }
-            if (!merged) groups.push_back({t, m});
+            if (!merged) groups.push_back({te, m});
         }
     };
-    assign(heads, da);
-    assign(2L * heads * (P - 1), dx);
+    assign(heads, a, false);
+    assign(2L * heads * (P - 1), x, true);
     return end;
 }
-
-// Predicted time of a split, in us, from measurements on a GB300 (152 SMs): a run takes
-// kRunUs plus kPeriodUs a chunk -- kPeriodFullUs for the later segments' runs when the
-// launch has more CTAs than SMs (they then share the GPU with every other run and were
-// measured slower) -- the combine step kCombUs plus kCombStepUs a step, and the correction
-// kCorrUs plus its bytes (C, out_0 and out: 768 a token) at kCorrBytesPerUs.  One pass:
-// kOnePeriodUs a chunk.
-constexpr double kPeriodUs = 2.95, kPeriodFullUs = 3.4, kRunUs = 4.0, kLaunchUs = 5.0;
-constexpr double kCombUs = 6.0, kCombStepUs = 3.0;
-constexpr double kCorrUs = 4.0, kCorrBytesPerUs = 6.2e6;
-constexpr double kOnePeriodUs = 2.8;
 
 SplitPlan plan_split_uncached(int heads, int S, int sms) {
     const int n = (S + kC - 1) / kC;
     SplitPlan best;
-    double best_us = 0.9 * (n * kOnePeriodUs + kLaunchUs);  // a split must save a tenth of one pass
-    for (int P = 2; P <= kMaxSegments; ++P) {
-        const double px = (long)heads * (2 * P - 1) > sms ? kPeriodFullUs : kPeriodUs;
+    double best_us = 0.9 * (n * kOnePeriodUs + kOneFixedUs);  // a split must save a tenth of one pass
+    for (int P = 2; P <= kMaxSegments; ++P)
         for (int x = 2; (long)(P - 1) * x < n; x += 2) {
             const int a = n - (P - 1) * x;
-            const double us = split_makespan(heads, sms, P, kRunUs + a * kPeriodUs, kRunUs + x * px) + kLaunchUs +
-                              kCombUs + (P - 1) * kCombStepUs + kCorrUs +
+            const double us = split_makespan(heads, sms, P, a, x) + kFixedUs + (P - 1) * kCombStepUs +
                               (double)heads * (S - a * kC) * 768.0 / kCorrBytesPerUs;
             if (us < best_us) {
                 best_us = us;
                 best = {P, a, x};
             }
         }
-    }
     return best;
 }
 

@@ -119,7 +119,8 @@ def test_prefill_segments():
     assert seg(4, 16, 32, 4096, sm_count=152) == 1        # 128 sequences: one pass
     assert seg(16, 8, 32, 2048, sm_count=152) == 1        # 512 sequences: one pass
     assert seg(1, 1, 2, 32768, sm_count=152) == 16        # capped by the run table
-    assert seg(2, 5, 25, 1536, sm_count=152) == 2         # 50 sequences: 150 CTAs in one wave
+    assert seg(2, 5, 25, 4096, sm_count=152) == 2         # 50 sequences: 150 CTAs in one wave
+    assert seg(2, 5, 25, 1536, sm_count=152) == 1         # 24 chunks: the split's fixed costs outweigh it
     assert seg(1, 1, 1, 256, sm_count=152) == 1           # 4 chunks: too short to pay
     assert seg(1, 1, 2, 32768, dtype=gdn.GDN_F32, sm_count=152) == 1
     assert seg(1, 1, 2, 32768, Dk=64, Dv=64, sm_count=152) == 1
@@ -138,12 +139,12 @@ def test_prefill_segment_starts():
     of one multiple of 128 tokens, the last one ending at S (ragged S included); one pass
     gives [0, S]; the count agrees with gdn_prefill_segments on every shape."""
     st = gdn.prefill_segment_starts
-    assert st(1, 16, 32, 32768, sm_count=152) == [0, 12288, 16384, 20480, 24576, 28672, 32768]
+    assert st(1, 16, 32, 32768, sm_count=152) == [0, 12928, 16896, 20864, 24832, 28800, 32768]
     assert st(4, 16, 32, 4096, sm_count=152) == [0, 4096]
     assert st(1, 1, 2, 4096, sm_count=152, single_pass=True) == [0, 4096]
     assert st(1, 2, 3, 4096, sm_count=152) == []
     for B, Hk, Hv, S in [(1, 1, 2, 2000), (1, 1, 1, 4608), (2, 2, 8, 3072), (1, 1, 2, 3000), (1, 2, 4, 2500),
-                         (2, 5, 25, 1536), (2, 4, 32, 8192), (1, 1, 8, 16385), (1, 1, 64, 32768), (1, 1, 2, 32767)]:
+                         (2, 5, 25, 4096), (2, 4, 32, 8192), (1, 1, 8, 16385), (1, 1, 64, 32768), (1, 1, 2, 32767)]:
         b = st(B, Hk, Hv, S, sm_count=152)
         assert len(b) - 1 == gdn.prefill_segments(B, Hk, Hv, S, sm_count=152) >= 2
         assert b[0] == 0 and b[-1] == S and all(x < y for x, y in zip(b, b[1:]))

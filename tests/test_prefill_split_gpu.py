@@ -45,8 +45,8 @@ CASES = [
     ("b1_hk2_hv4_s2500_strong_decay", 1, 2, 4, 2500, 0.05, (-2.0, -0.001), 2.0, 105),
     # almost no decay: the state persists through every segment, so the maps carry it
     ("b1_hv2_s4096_almost_no_decay", 1, 1, 2, 4096, 0.05, (-1e-4, -1e-6), 1.0, 107),
-    # 50 sequences (two segments: 150 CTAs in one wave) and 24 chunks
-    ("b2_hk5_hv25_s1536_two_segments", 2, 5, 25, 1536, 0.02, (-0.5, -0.005), 1.0, 106),
+    # 50 sequences: two segments, 150 CTAs in one wave
+    ("b2_hk5_hv25_s4096_two_segments", 2, 5, 25, 4096, 0.02, (-0.5, -0.005), 1.0, 106),
     # 64 sequences: the runs take two waves of CTAs
     ("b2_hk4_hv32_s8192_two_waves", 2, 4, 32, 8192, 0.02, (-0.5, -0.005), 1.0, 108),
 ]
