@@ -486,8 +486,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             fetch_decays(1, pt - 128);
         }
         // chunk 0's decays are read by every prep thread (masks, Q'): the chunk's input load
-        // alone does not order them after the scan (it may land first, from L2)
-        named_bar_sync(BAR_PREP, kPrep);
+        // alone does not order them after the scan (it may land first, from L2), so a prep
+        // barrier does -- here, or just before chunk 0's masks.  Either is correct; here was
+        // measured faster for launches of several CTA waves (3-4 %) and the later place for
+        // one wave (4 %), so each instantiation takes its own.
+        constexpr bool kEarlyBar = kSplit || kQSplit;
+        if (kEarlyBar) named_bar_sync(BAR_PREP, kPrep);
         for (int c = 0; c < n_chunks; ++c) {
             const int s = c % kStages;  // input stage
             uint8_t* st = sm + s * STAGE_BYTES;
@@ -503,6 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (!fail) fail = !mbar_wait_or_abort(&bars->gram, c & 1, abort_flag);
             if (!fail) gram_waited = c;
+            if (!kEarlyBar && c == 0) named_bar_sync(BAR_PREP, kPrep);  // chunk 0's decays, see above
             tc_fence_after();
 
             // ---- P (bf16, lanes 0..63) and A (fp32, lanes 64..127); 32 columns per thread
