@@ -1365,7 +1365,8 @@ constexpr int kMaxSegments = (kMaxRuns + 1) / 2;
 // 2 to 12 segments for 32 and 64 sequences of 8192 and 32768 tokens; within 3 % on the 32768
 // ones).  A run costs kRunUs plus a period per chunk: kPeriodAUs for segment 0; for the
 // later segments' runs from kPeriodLoUs up to kPeriodHiUs as the CTAs running at their start
-// go from 128 to 152 (measured: the more CTAs run, the slower each one).  Then the combine
+// go from 128 to 152 of 152 SMs (measured: the more CTAs run, the slower each one; taken
+// as the same fractions of the SM count elsewhere).  Then the combine
 // (kCombStepUs a step), the correction (768 bytes a token -- C, out_0 and out -- at
 // kCorrBytesPerUs) and kFixedUs for the launches.  One pass: kOnePeriodUs a chunk.
 constexpr double kPeriodAUs = 2.95, kPeriodLoUs = 2.8, kPeriodHiUs = 3.3, kRunUs = 2.0;
@@ -1390,7 +1391,7 @@ double split_makespan(int heads, int sms, int P, int a, int x) {
                 if (g.first > t) busy += g.second;
             double period = kPeriodAUs;
             if (later) {
-                const double f = (double)(busy - 128) / 24.0;
+                const double f = ((double)busy / sms - 128.0 / 152.0) / (24.0 / 152.0);
                 period = kPeriodLoUs + (kPeriodHiUs - kPeriodLoUs) * (f < 0.0 ? 0.0 : f > 1.0 ? 1.0 : f);
             }
             const double te = t + kRunUs + chunks * period;
