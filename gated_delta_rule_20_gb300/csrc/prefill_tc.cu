@@ -848,7 +848,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // that the reload does not wait behind thread 0's output product and store); the last
         // load this thread issued
         int last_load = -1;
-        // v of the run (a map run of a split reads the zero tile for every chunk)
+        // v of the run (a split's identity-start runs read the zero tile for every chunk)
         const bool zero_v = kSplit && runs.run[ri].zero_v;
         const CUtensorMap* tv_run = zero_v ? &tm_v0 : &tm_v;
         const int vh = zero_v ? 0 : bh;
