@@ -155,6 +155,32 @@ def test_prefill_segment_starts():
             assert 0 < S - b[-2] <= b[2] - b[1]   # the last segment: at most one middle segment
 
 
+def test_prefill_split_plans_are_valid():
+    """Every plan the split rule returns (host only, many shapes and SM counts) tiles the
+    sequence: segment 0 of whole chunks, the middle segments of one length in whole
+    128-token tiles, the last one no longer than them and ending at S, at most 16 segments;
+    and the same dims ask for the same plan again."""
+    import random
+    rng = random.Random(5)
+    st = gdn.prefill_segment_starts
+    for _ in range(300):
+        Hk = rng.choice([1, 2, 4, 8, 16])
+        Hv = Hk * rng.choice([1, 2, 4])
+        B = rng.choice([1, 1, 2, 3, 4])
+        S = rng.choice([rng.randint(1, 4096), rng.randint(4096, 70000)])
+        sms = rng.choice([132, 148, 152])
+        b = st(B, Hk, Hv, S, sm_count=sms)
+        P = len(b) - 1
+        assert P == gdn.prefill_segments(B, Hk, Hv, S, sm_count=sms) and 1 <= P <= 16
+        assert b[0] == 0 and b[-1] == S and all(x < y for x, y in zip(b, b[1:]))
+        if P > 1:
+            assert b[1] % 64 == 0
+            lens = [y - x for x, y in zip(b[1:], b[2:])]
+            assert all(m == lens[0] and m % 128 == 0 for m in lens[:-1])
+            assert 0 < lens[-1] <= lens[0] if len(lens) > 1 else lens[0] > 0
+        assert st(B, Hk, Hv, S, sm_count=sms) == b
+
+
 def test_prefill_flags_known(L):
     # every documented flag passes validation (B = 0: no CUDA call); the next bit does not
     for f in (gdn.GDN_ZERO_INITIAL_STATE, gdn.GDN_FORCE_FFMA, gdn.GDN_SINGLE_PASS,
