@@ -112,8 +112,9 @@ typedef struct {
  * affine in its start state: a later segment's end state is M S0 + X and its
  * output at token t is out_0[t] + C[t] S0, with X and out_0 its end state and
  * outputs from a zero start and M and C (C[t]: 1 x Dk per token) its end state
- * and outputs from S0 = I with v = 0.  Five launches: an identity matrix; one
- * launch of segment 0 from the real start state and both runs of every later
+ * and outputs from S0 = I with v = 0.  Four kernel launches and a memset: an
+ * identity matrix and a zero v tile; one launch of segment 0 from the real
+ * start state and both runs of every later
  * segment (out_0 is written to out, C to the scratch); a combine step that
  * chains the maps into every segment's start state and the final state
  * (fp32); a correction that adds C[t] S0 to the later segments' outputs
@@ -121,9 +122,9 @@ typedef struct {
  * (gdn_prefill_workspace_bytes: 3 (P - 1) states per sequence, one identity,
  * and C for every token after segment 0) is allocated with cudaMallocAsync on
  * `stream` and freed there; if that allocation fails, the call runs one pass
- * instead.  The results agree with the one-pass form to within rounding (the
- * same error against an fp64 reference, from strong decay to none), not bit for
- * bit; segment 0's outputs are those of one pass.
+ * instead.  The results agree with the one-pass form to within rounding (a
+ * similar error against an fp64 reference, from strong decay to none), not bit
+ * for bit; segment 0's outputs are those of one pass.
  */
 gdn_status gdn_prefill(const void* q, const void* k, const void* v,
                        const float* g_log, const float* beta, float scale,
